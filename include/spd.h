@@ -1,0 +1,201 @@
+/*
+ * spd.h -- C ABI of the GB300 (sm_103a) sample-packing and document-masked
+ * attention library (libspd.so).
+ *
+ * Three operations, one per step of the packed-training hot path:
+ *
+ *   spd_pack_tokens      token lists -> packed rows: input_ids, labels,
+ *                        indexes, cu_seqlens, max_seqlen
+ *                        (InternEvo page "Data loading and flow", sections
+ *                        "Dataloader loading data" and "Fetching data from the
+ *                        Dataloader").
+ *   spd_varlen_attn_fwd  causal attention over packed rows with the
+ *                        block-diagonal (per-document causal) mask given by
+ *                        cu_seqlens (page "Sample Packing: attention problems of
+ *                        long-sequence LLM training", sections 3 "Attention
+ *                        Mask" and 5.1 "FlashAttention", the varlen split into
+ *                        one causal attention per document).
+ *   spd_varlen_attn_bwd  its exact gradient (dQ, dK, dV).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are DEVICE pointers unless the argument says "host". The caller
+ *   owns and allocates all memory (inputs, outputs and workspace); the library
+ *   allocates nothing and keeps no global state beyond a per-device cache of
+ *   the SM count. Entry points are thread-safe.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream). The return value reports what the host can check before launch.
+ *   Errors the GPU finds (bad cu_seqlens, bad document lengths, a bounded
+ *   wait that ran out) are written to a status word at the start of the
+ *   workspace; spd_read_status() synchronises the stream and returns it. Each
+ *   call clears the status word first, so it reports the most recent call
+ *   that used that workspace. No kernel traps; on a device error the kernels
+ *   finish early and the outputs are unspecified.
+ * - Workspaces must be at least the size the matching *_workspace_size()
+ *   returns and 256-byte aligned. Calls that share a workspace must not
+ *   overlap on the GPU (use one stream, or one workspace per stream).
+ * - All integer outputs are int32 (the page prints torch tensors; values are
+ *   identical). Pad id is 0 and the ignore label is -100.
+ */
+#ifndef SPD_H
+#define SPD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *spd_stream_t; /* same type as cudaStream_t */
+
+enum {
+    SPD_OK = 0,
+    SPD_ERR_INVALID_ARG = -1,    /* host: null/misaligned pointer, bad size or shape */
+    SPD_ERR_UNSUPPORTED = -2,    /* host: head_dim or GPU not supported */
+    SPD_ERR_CUDA = -3,           /* host: a CUDA runtime/driver call failed */
+    SPD_ERR_BAD_SEQLENS = -4,    /* device: cu_seqlens not 0 = c0 < c1 < ... = total */
+    SPD_ERR_DEVICE_TIMEOUT = -5, /* device: a bounded wait ran out */
+    SPD_ERR_WORKSPACE = -6,      /* host: workspace too small or misaligned */
+    SPD_ERR_BAD_DOCS = -7        /* device: a document length <= 0 or sum != num_tokens */
+};
+
+/* Text for a status code (static storage). */
+const char *spd_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int spd_version(void);
+
+/*
+ * Synchronise `stream` and return the device status word of the last call
+ * that used workspace `ws` (SPD_OK or a negative SPD_ERR_* code) in
+ * *device_status (host). Returns SPD_OK or SPD_ERR_CUDA.
+ */
+int spd_read_status(const void *ws, spd_stream_t stream, int *device_status);
+
+/* ------------------------------------------------------------------------- */
+/* Packing                                                                   */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Output sizes of spd_pack_tokens (all host arguments and results).
+ *   use_packed_dataset != 0 (build_pack): rows = ceil(num_tokens / plen),
+ *   use_packed_dataset == 0 (build_unpack): rows = ceil(num_docs / micro_bsz),
+ *   with plen = micro_bsz * seq_len. *max_segs bounds num_segs: size
+ *   cu_seqlens with max_segs + 1 entries. Returns SPD_ERR_INVALID_ARG if a
+ *   size is <= 0 (num_docs / num_tokens may be 0) or rows * plen does not fit
+ *   in int32.
+ */
+int spd_pack_rows(int64_t num_docs, int64_t num_tokens, int micro_bsz, int seq_len,
+                  int use_packed_dataset, int64_t *rows, int64_t *max_segs);
+
+/* Workspace bytes spd_pack_tokens needs for num_docs documents. */
+size_t spd_pack_workspace_size(int64_t num_docs);
+
+/*
+ * Pack documents into rows of plen = micro_bsz * seq_len tokens.
+ *
+ * Follows the InternEvo page "Data loading and flow", section "Dataloader
+ * loading data":
+ *   use_packed_dataset != 0 (build_pack): the documents are laid end to end
+ *     and cut every plen tokens; a document that does not fit continues at the
+ *     start of the next row; the last row is padded with 0. Each document's
+ *     labels are its tokens from the second on followed by -100, taken before
+ *     the cut (so a row's last label may be the next row's first token);
+ *     padding labels are -100.
+ *   use_packed_dataset == 0 (build_unpack): at most micro_bsz documents per
+ *     row; each is cut to seq_len tokens and the excess dropped; labels come
+ *     from the cut document; rows are padded with 0 / -100.
+ * and section "Fetching data from the Dataloader" for the segment fields:
+ *   segments of a row are the runs of one document's tokens, then the padding
+ *   tail as its own segment; indexes[p] is p's position inside its segment
+ *   (restarting at 0 at every segment start, padding included); max_seqlen[r]
+ *   is the longest segment of row r.
+ *
+ * Inputs (device): tokens int32 [num_tokens] (the documents concatenated),
+ *   doc_lens int32 [num_docs], each >= 1, summing to num_tokens (checked on
+ *   the GPU: SPD_ERR_BAD_DOCS).
+ * Outputs (device), with rows from spd_pack_rows:
+ *   input_ids, labels, indexes  int32 [rows * plen], row-major;
+ *   cu_seqlens   int32 [num_segs + 1], GLOBAL token offsets: row r's
+ *                boundaries plus r * plen, each shared row end once, so
+ *                cu_seqlens is directly the attention calls' argument;
+ *   row_seg_ptr  int32 [rows + 1]: row r's segments are
+ *                cu_seqlens[row_seg_ptr[r] .. row_seg_ptr[r+1]];
+ *   max_seqlen   int32 [rows];
+ *   num_segs     int32 [1].
+ * Any output pointer may be unaligned; 16-byte aligned outputs take the
+ * vectorised store path. Returns SPD_ERR_INVALID_ARG / SPD_ERR_WORKSPACE /
+ * SPD_ERR_CUDA from the host; device errors go to the status word.
+ */
+int spd_pack_tokens(const int32_t *tokens, const int32_t *doc_lens, int64_t num_docs,
+                    int64_t num_tokens, int micro_bsz, int seq_len, int use_packed_dataset,
+                    int32_t *input_ids, int32_t *labels, int32_t *indexes, int32_t *cu_seqlens,
+                    int32_t *row_seg_ptr, int32_t *max_seqlen, int32_t *num_segs, void *ws,
+                    size_t ws_bytes, spd_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Attention                                                                 */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Workspace bytes for spd_varlen_attn_fwd (bwd == 0) or spd_varlen_attn_bwd
+ * (bwd != 0). The backward workspace holds an fp32 dQ accumulator of
+ * Hq * total_tokens * head_dim floats plus the row terms D = rowsum(dO * O).
+ * Returns 0 for unsupported arguments.
+ */
+size_t spd_attn_workspace_size(int64_t total_tokens, int32_t num_segs, int Hq, int Hkv,
+                               int head_dim, int bwd);
+
+/*
+ * Forward attention over packed rows.
+ *
+ * For every segment s = [a, b) of cu_seqlens, q head h and token i in s, with
+ * kv head g = h / (Hq / Hkv) (GQA: consecutive q heads share a kv head, the
+ * InternEvo page "Data loading and flow", section "Computing attention"):
+ *   S_ij = softmax_scale * q[i,h,:] . k[j,g,:]   for a <= j <= i
+ *   out[i,h,:] = sum_j softmax_j(S_i.) v[j,g,:],  lse[h,i] = log sum_j exp(S_ij)
+ * Segments never interact: a packed row gives the same result as its documents
+ * attended separately (page "Sample Packing ...", section 3 "Attention Mask").
+ * Only the tiles of each document's own causal triangle are visited (section
+ * 5.1 "FlashAttention"); the varlen split makes every document its own
+ * causal attention.
+ *
+ * Inputs (device, contiguous, bf16 as uint16 bit patterns, 16-byte aligned):
+ *   q [total_tokens, Hq, head_dim], k, v [total_tokens, Hkv, head_dim];
+ *   cu_seqlens int32 [num_segs + 1], 0 = c0 < c1 < ... < c_num_segs =
+ *   total_tokens (checked on the GPU: SPD_ERR_BAD_SEQLENS);
+ *   max_seqlen (host) bounds the longest segment (a hint; <= 0 = unknown).
+ * head_dim is 64 or 128; Hq % Hkv == 0; softmax_scale <= 0 means
+ * 1 / sqrt(head_dim).
+ * Outputs (device): out bf16 [total_tokens, Hq, head_dim]; lse fp32
+ *   [Hq, total_tokens] (natural log).
+ */
+int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
+                        int32_t max_seqlen, int Hq, int Hkv, int head_dim, float softmax_scale,
+                        uint16_t *out, float *lse, void *ws, size_t ws_bytes,
+                        spd_stream_t stream);
+
+/*
+ * Backward of spd_varlen_attn_fwd: with P_ij = exp(S_ij - lse_i),
+ * D_i = dout_i . out_i and dS_ij = P_ij (dout_i . v_j - D_i):
+ *   dq_i = scale sum_j dS_ij k_j,
+ *   dk_j = scale sum_{h in g} sum_i dS_ij q_i,
+ *   dv_j = sum_{h in g} sum_i P_ij dout_i.
+ * Inputs as for the forward plus out (bf16), dout (bf16) [total_tokens, Hq,
+ * head_dim] and the forward's lse. grad_dtype 0 writes dq / dk / dv as bf16
+ * (uint16 bit patterns), 1 as fp32; shapes [total_tokens, Hq | Hkv, head_dim].
+ */
+int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const uint16_t *out, const uint16_t *dout, const float *lse,
+                        const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
+                        int32_t max_seqlen, int Hq, int Hkv, int head_dim, float softmax_scale,
+                        int grad_dtype, void *dq, void *dk, void *dv, void *ws,
+                        size_t ws_bytes, spd_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPD_H */

@@ -1,0 +1,313 @@
+// C-ABI front end (include/spd.h): argument checks, workspace carving, TMA
+// tensor maps, kernel launches. No allocation, no synchronisation except in
+// spd_read_status.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/spd.h"
+#include "internal.h"
+
+namespace spd {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];
+std::atomic<int> g_cc[kMaxDevices];
+
+// SM count and compute capability (major * 10 + minor) of the current device.
+int device_info(int *sms, int *cc)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPD_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices && g_sms[dev].load() > 0) {
+        *sms = g_sms[dev].load();
+        *cc = g_cc[dev].load();
+        return SPD_OK;
+    }
+    int n = 0, ma = 0, mi = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return SPD_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevices) {
+        g_cc[dev].store(ma * 10 + mi);
+        g_sms[dev].store(n);
+    }
+    *sms = n;
+    *cc = ma * 10 + mi;
+    return SPD_OK;
+}
+
+int require_sm103(int *sms)
+{
+    int cc = 0;
+    int rc = device_info(sms, &cc);
+    if (rc != SPD_OK) return rc;
+    return cc == 103 ? SPD_OK : SPD_ERR_UNSUPPORTED;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn()
+{
+    static std::atomic<EncodeTiled> fn{nullptr};
+    EncodeTiled f = fn.load();
+    if (f) return f;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+        return nullptr;
+    f = reinterpret_cast<EncodeTiled>(p);
+    fn.store(f);
+    return f;
+}
+
+// Tensor map over a [T, H, D] bf16 array: dims (D, H, T), box (64, 1, 128),
+// 128-byte swizzle; rows past T read as zero.
+int make_map(CUtensorMap *m, const void *base, int64_t T, int H, int D)
+{
+    EncodeTiled f = encode_fn();
+    if (!f) return SPD_ERR_CUDA;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SPD_OK : SPD_ERR_CUDA;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SPD_OK : SPD_ERR_CUDA; }
+
+int check_attn_shape(int64_t T, int32_t num_segs, int Hq, int Hkv, int D)
+{
+    if (D != 64 && D != 128) return SPD_ERR_UNSUPPORTED;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return SPD_ERR_INVALID_ARG;
+    if (T < 0 || T > 0x7fffffffLL || num_segs < 0 || num_segs > T) return SPD_ERR_INVALID_ARG;
+    if ((T > 0) != (num_segs > 0)) return SPD_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(Hq) * T > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    return SPD_OK;
+}
+
+size_t bwd_delta_off(int64_t T, int32_t num_segs) { return align_up(schedule_ws_bytes(T, num_segs), 256); }
+size_t bwd_acc_off(int64_t T, int32_t num_segs, int Hq)
+{
+    return bwd_delta_off(T, num_segs) + align_up(sizeof(float) * static_cast<size_t>(Hq) * T, 256);
+}
+
+int clear_status(void *ws, cudaStream_t stream)
+{
+    return cuda_rc(cudaMemsetAsync(ws, 0, sizeof(int), stream));
+}
+
+}  // namespace
+}  // namespace spd
+
+using namespace spd;
+
+extern "C" {
+
+const char *spd_status_string(int s)
+{
+    switch (s) {
+    case SPD_OK: return "ok";
+    case SPD_ERR_INVALID_ARG: return "invalid argument";
+    case SPD_ERR_UNSUPPORTED: return "unsupported (head_dim or GPU)";
+    case SPD_ERR_CUDA: return "CUDA error";
+    case SPD_ERR_BAD_SEQLENS: return "cu_seqlens is not 0 = c0 < c1 < ... = total_tokens";
+    case SPD_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
+    case SPD_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case SPD_ERR_BAD_DOCS: return "a document length <= 0 or lengths do not sum to num_tokens";
+    default: return "unknown status";
+    }
+}
+
+int spd_version(void) { return 100; }
+
+int spd_read_status(const void *ws, spd_stream_t stream, int *device_status)
+{
+    if (!ws || !device_status) return SPD_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return SPD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SPD_ERR_CUDA;
+    *device_status = v;
+    return SPD_OK;
+}
+
+int spd_pack_rows(int64_t num_docs, int64_t num_tokens, int micro_bsz, int seq_len, int use_packed_dataset,
+                  int64_t *rows, int64_t *max_segs)
+{
+    if (!rows || !max_segs) return SPD_ERR_INVALID_ARG;
+    if (micro_bsz <= 0 || seq_len <= 0 || num_docs < 0 || num_tokens < 0) return SPD_ERR_INVALID_ARG;
+    if (num_docs > 0x7fffffffLL || num_tokens > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if ((num_docs == 0) != (num_tokens == 0)) return SPD_ERR_INVALID_ARG;
+    const int64_t plen = static_cast<int64_t>(micro_bsz) * seq_len;
+    const int64_t r = use_packed_dataset ? (num_tokens + plen - 1) / plen : (num_docs + micro_bsz - 1) / micro_bsz;
+    if (r * plen > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    *rows = r;
+    *max_segs = num_docs + 2 * r;
+    if (*max_segs > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    return SPD_OK;
+}
+
+size_t spd_pack_workspace_size(int64_t num_docs)
+{
+    if (num_docs < 0) return 0;
+    return pack_ws_bytes(num_docs);
+}
+
+int spd_pack_tokens(const int32_t *tokens, const int32_t *doc_lens, int64_t num_docs, int64_t num_tokens,
+                    int micro_bsz, int seq_len, int use_packed_dataset, int32_t *input_ids, int32_t *labels,
+                    int32_t *indexes, int32_t *cu_seqlens, int32_t *row_seg_ptr, int32_t *max_seqlen,
+                    int32_t *num_segs, void *ws, size_t ws_bytes, spd_stream_t stream)
+{
+    int64_t rows = 0, max_segs = 0;
+    int rc = spd_pack_rows(num_docs, num_tokens, micro_bsz, seq_len, use_packed_dataset, &rows, &max_segs);
+    if (rc != SPD_OK) return rc;
+    if (!ws || !aligned(ws, 256)) return SPD_ERR_WORKSPACE;
+    if (ws_bytes < spd_pack_workspace_size(num_docs)) return SPD_ERR_WORKSPACE;
+    if (!cu_seqlens || !row_seg_ptr || !num_segs) return SPD_ERR_INVALID_ARG;
+    if (rows > 0 && (!input_ids || !labels || !indexes || !max_seqlen)) return SPD_ERR_INVALID_ARG;
+    if (num_docs > 0 && (!tokens || !doc_lens)) return SPD_ERR_INVALID_ARG;
+    const void *ptrs[] = {tokens, doc_lens, input_ids, labels, indexes, cu_seqlens, row_seg_ptr, max_seqlen, num_segs};
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 4)) return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+
+    PackArgs a = {};
+    a.tokens = tokens;
+    a.doc_lens = doc_lens;
+    a.num_docs = static_cast<int32_t>(num_docs);
+    a.num_tokens = static_cast<int32_t>(num_tokens);
+    a.micro_bsz = micro_bsz;
+    a.seq_len = seq_len;
+    a.plen = micro_bsz * seq_len;
+    a.rows = static_cast<int32_t>(rows);
+    a.packed = use_packed_dataset ? 1 : 0;
+    a.input_ids = input_ids;
+    a.labels = labels;
+    a.indexes = indexes;
+    a.cu_seqlens = cu_seqlens;
+    a.row_seg_ptr = row_seg_ptr;
+    a.max_seqlen = max_seqlen;
+    a.num_segs = num_segs;
+    a.status = static_cast<int *>(ws);
+    a.vec_out = aligned(input_ids, 16) && aligned(labels, 16) && aligned(indexes, 16);
+    a.vec_in = aligned(tokens, 16);
+    return cuda_rc(launch_pack(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t spd_attn_workspace_size(int64_t total_tokens, int32_t num_segs, int Hq, int Hkv, int head_dim, int bwd)
+{
+    if (check_attn_shape(total_tokens, num_segs, Hq, Hkv, head_dim) != SPD_OK) return 0;
+    if (!bwd) return schedule_ws_bytes(total_tokens, num_segs);
+    return bwd_acc_off(total_tokens, num_segs, Hq) +
+           align_up(sizeof(float) * static_cast<size_t>(Hq) * total_tokens * head_dim, 256);
+}
+
+int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                        int32_t num_segs, int64_t total_tokens, int32_t max_seqlen, int Hq, int Hkv, int head_dim,
+                        float softmax_scale, uint16_t *out, float *lse, void *ws, size_t ws_bytes,
+                        spd_stream_t stream)
+{
+    (void)max_seqlen;
+    int rc = check_attn_shape(total_tokens, num_segs, Hq, Hkv, head_dim);
+    if (rc != SPD_OK) return rc;
+    if (!ws || !aligned(ws, 256)) return SPD_ERR_WORKSPACE;
+    if (ws_bytes < spd_attn_workspace_size(total_tokens, num_segs, Hq, Hkv, head_dim, 0)) return SPD_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (total_tokens == 0) return clear_status(ws, s);
+    if (!q || !k || !v || !out || !lse || !cu_seqlens) return SPD_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        !aligned(cu_seqlens, 4))
+        return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
+
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, ws, s));
+    if (rc != SPD_OK) return rc;
+    AttnFwdArgs a = {};
+    if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_k, k, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_v, v, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
+    char *base = static_cast<char *>(ws);
+    a.out = out;
+    a.lse = lse;
+    a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
+    a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
+    a.status = reinterpret_cast<int *>(base);
+    a.total_tokens = static_cast<int32_t>(total_tokens);
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.scale = softmax_scale;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    return cuda_rc(launch_attn_fwd(a, head_dim, max_tiles(total_tokens, num_segs), s));
+}
+
+int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *out,
+                        const uint16_t *dout, const float *lse, const int32_t *cu_seqlens, int32_t num_segs,
+                        int64_t total_tokens, int32_t max_seqlen, int Hq, int Hkv, int head_dim,
+                        float softmax_scale, int grad_dtype, void *dq, void *dk, void *dv, void *ws,
+                        size_t ws_bytes, spd_stream_t stream)
+{
+    (void)max_seqlen;
+    int rc = check_attn_shape(total_tokens, num_segs, Hq, Hkv, head_dim);
+    if (rc != SPD_OK) return rc;
+    if (grad_dtype != 0 && grad_dtype != 1) return SPD_ERR_INVALID_ARG;
+    if (!ws || !aligned(ws, 256)) return SPD_ERR_WORKSPACE;
+    if (ws_bytes < spd_attn_workspace_size(total_tokens, num_segs, Hq, Hkv, head_dim, 1)) return SPD_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (total_tokens == 0) return clear_status(ws, s);
+    if (!q || !k || !v || !out || !dout || !lse || !cu_seqlens || !dq || !dk || !dv) return SPD_ERR_INVALID_ARG;
+    const void *p16[] = {q, k, v, out, dout, dq, dk, dv};
+    for (const void *p : p16)
+        if (!aligned(p, 16)) return SPD_ERR_INVALID_ARG;
+    if (!aligned(lse, 4) || !aligned(cu_seqlens, 4)) return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
+
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 1, ws, s));
+    if (rc != SPD_OK) return rc;
+    AttnBwdArgs a = {};
+    if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_k, k, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_v, v, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_do, dout, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
+    char *base = static_cast<char *>(ws);
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.delta = reinterpret_cast<float *>(base + bwd_delta_off(total_tokens, num_segs));
+    a.dq_acc = reinterpret_cast<float *>(base + bwd_acc_off(total_tokens, num_segs, Hq));
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.grad_fp32 = grad_dtype;
+    a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
+    a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
+    a.status = reinterpret_cast<int *>(base);
+    a.total_tokens = static_cast<int32_t>(total_tokens);
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.scale = softmax_scale;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    return cuda_rc(launch_attn_bwd(a, head_dim, max_tiles(total_tokens, num_segs), s));
+}
+
+}  // extern "C"

@@ -1,0 +1,522 @@
+// Backward of the document-masked causal attention.
+//
+// With P_ij = exp(S_ij - LSE_i), D_i = dO_i . O_i and dS_ij = P_ij (dP_ij - D_i),
+// dP_ij = dO_i . v_j (the exact gradient of the masked softmax):
+//   dV_j = sum_i P_ij dO_i,   dK_j = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j,
+// summed over the q heads that share a kv head (GQA). As in the forward pass,
+// only tiles inside a document's own causal triangle are visited (page "Sample
+// Packing: attention problems of long-sequence LLM training", section 5.1
+// "FlashAttention").
+//
+// Three launches:
+//   bwd_pre_kernel   D_i = rowsum(dO * O) (fp32) and zeroes the fp32 dQ
+//                    accumulator [Hq, T, d].
+//   attn_bwd_kernel  one CTA per (128-row kv tile, kv head): K, V stay in shared
+//                    memory; the CTA walks every (q head of the group, q tile
+//                    from the diagonal to the segment end). Per step, five
+//                    tcgen05 MMAs with fp32 accumulation in TMEM:
+//                      S^T = K Q^T, dP^T = V dO^T        (TMEM, 128 x 128)
+//                      dV += P^T dO, dK += dS^T Q        (TMEM accumulators)
+//                      dQ_part = dS K                    (TMEM, then red.add to HBM)
+//                    P^T and dS^T go through one bf16 shared-memory buffer; the
+//                    dQ MMA reads dS^T back as an M-major operand, so dS is
+//                    written once.
+//   bwd_dq_kernel    dq = scale * accumulator, in the output layout and type.
+//
+// Warp roles of attn_bwd_kernel (192 threads): warps 0-3 compute (thread t owns
+// kv row t = TMEM lane t for S^T / dP^T / dK / dV, and q row t for the dQ
+// readout), warp 4 TMA producer, warp 5 MMA issuer.
+// TMEM: S^T and then dQ [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d).
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace spd {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAtom = 128 * 128;
+constexpr int kQStages = 2;
+
+template <int D>
+struct BwdSmem {
+    uint8_t k[D / 64][kAtom];
+    uint8_t v[D / 64][kAtom];
+    uint8_t q[kQStages][D / 64][kAtom];
+    uint8_t dout[kQStages][D / 64][kAtom];
+    uint8_t pds[2][kAtom];           // P^T, then dS^T: [128 kv rows][128 q cols]
+    float lse2[2][128];              // LSE * log2(e) of the step's q columns
+    float delta[2][128];             // D of the step's q columns
+    uint64_t kv_full;
+    uint64_t q_full[kQStages], q_empty[kQStages], do_full[kQStages], do_empty[kQStages];
+    uint64_t s_full, dp_full, dp_free, p_full, dv_done, ds_full, pds_free, dq_full, dq_free;
+    uint64_t cols[2];                // the step's lse2 / delta written (128 arrivals)
+    uint64_t fin, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_drain(uint64_t *bar, uint32_t parity)
+{
+    uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int *status)
+{
+    bool w = mbar_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, w);
+}
+
+__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Writes one 128-column bf16 row (64 packed words) into a [128][128] tile of
+// two 128-byte-swizzled atoms.
+__device__ __forceinline__ void store_row_sw128(uint32_t tile_addr, int row, const uint32_t (&pk)[64])
+{
+    const uint32_t base = tile_addr + row * 128;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const uint32_t addr = base + (c >> 3) * kAtom + (((c & 7) ^ (row & 7)) << 4);
+        st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    }
+}
+
+// ------------------------------------------------------------------ preprocess
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict__ out,
+                                                      const uint16_t *__restrict__ dout, float *delta,
+                                                      float *dq_acc, int32_t T, int32_t Hq)
+{
+    // 8 threads per (token, head) row; each covers D / 8 elements. A warp
+    // takes 4 rows per iteration and every lane runs the same iterations, so
+    // the 8-lane shuffles always see a full warp.
+    constexpr int kPer = D / 8;
+    const long long rows = static_cast<long long>(T) * Hq;
+    const int lane = threadIdx.x & 31, sub = lane & 7;
+    const long long warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+    for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w * 4 < rows;
+         w += warps) {
+        const long long row = w * 4 + (lane >> 3);
+        const bool active = row < rows;
+        float acc = 0.f;
+        if (active) {
+            const uint4 *o4 = reinterpret_cast<const uint4 *>(out + row * D + sub * kPer);
+            const uint4 *d4 = reinterpret_cast<const uint4 *>(dout + row * D + sub * kPer);
+#pragma unroll
+            for (int c = 0; c < kPer / 8; ++c) {
+                uint4 a = o4[c], b = d4[c];
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc += bf16_lo(aw[e]) * bf16_lo(bw[e]) + bf16_hi(aw[e]) * bf16_hi(bw[e]);
+            }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        if (!active) continue;
+        const long long i = row / Hq;
+        const int h = static_cast<int>(row % Hq);
+        const long long hi = static_cast<long long>(h) * T + i;
+        if (sub == 0) delta[hi] = acc;
+        float4 *z = reinterpret_cast<float4 *>(dq_acc + hi * D + sub * kPer);
+#pragma unroll
+        for (int c = 0; c < kPer / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// ------------------------------------------------------------------ dq convert
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ dq_acc, void *dq,
+                                                     int grad_fp32, float scale, int32_t T, int32_t Hq)
+{
+    // one thread per 8 consecutive elements of one (token, head) row
+    const long long n8 = static_cast<long long>(T) * Hq * (D / 8);
+    for (long long x = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; x < n8;
+         x += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = x / (D / 8);  // token-major row = i * Hq + h
+        const int c8 = static_cast<int>(x % (D / 8));
+        const long long i = row / Hq;
+        const int h = static_cast<int>(row % Hq);
+        const float4 *src = reinterpret_cast<const float4 *>(dq_acc + (static_cast<long long>(h) * T + i) * D + c8 * 8);
+        float4 a = src[0], b = src[1];
+        float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        if (grad_fp32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(dq) + row * D + c8 * 8);
+            dst[0] = make_float4(v[0] * scale, v[1] * scale, v[2] * scale, v[3] * scale);
+            dst[1] = make_float4(v[4] * scale, v[5] * scale, v[6] * scale, v[7] * scale);
+        } else {
+            uint4 w = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
+                                 pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dq) + row * D + c8 * 8) = w;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ main kernel
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ AttnBwdArgs a)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    BwdSmem<D> &sm = *reinterpret_cast<BwdSmem<D> *>(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (*reinterpret_cast<volatile int *>(a.status) != 0) return;
+    if (smem_u32(smem_raw) & 1023u) {  // swizzled operand atoms need 1024-byte alignment
+        if (threadIdx.x == 0) set_status(a.status, kErrTimeout);
+        return;
+    }
+    const int tile_idx = blockIdx.x / a.Hkv;
+    const int g = blockIdx.x % a.Hkv;
+    if (tile_idx >= *a.tile_count) return;
+    const Tile tl = a.tiles[tile_idx];
+    const int group = a.Hq / a.Hkv;
+    const int n_seg_tiles = (tl.seg_end - tl.seg_start + kTile - 1) / kTile;
+    const int nq = n_seg_tiles - tl.t;   // q tiles t .. n-1
+    const int nsteps = group * nq;
+    const int k0 = tl.seg_start + tl.t * kTile;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.kv_full, 1);
+        for (int s = 0; s < kQStages; ++s) {
+            mbar_init(&sm.q_full[s], 1);
+            mbar_init(&sm.q_empty[s], 1);
+            mbar_init(&sm.do_full[s], 1);
+            mbar_init(&sm.do_empty[s], 1);
+        }
+        mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.dp_full, 1);
+        mbar_init(&sm.dp_free, 128);
+        mbar_init(&sm.p_full, 128);
+        mbar_init(&sm.dv_done, 1);
+        mbar_init(&sm.ds_full, 128);
+        mbar_init(&sm.pds_free, 1);
+        mbar_init(&sm.dq_full, 1);
+        mbar_init(&sm.dq_free, 128);
+        mbar_init(&sm.cols[0], 128);
+        mbar_init(&sm.cols[1], 128);
+        mbar_init(&sm.fin, 1);
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&a.tm_q);
+        tma_prefetch_desc(&a.tm_k);
+        tma_prefetch_desc(&a.tm_v);
+        tma_prefetch_desc(&a.tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    volatile int *abort_flag = &sm.abort_flag;
+    constexpr uint32_t kTileBytes = 128 * D * 2;
+    constexpr uint32_t kDV = 256, kDK = 256 + D;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
+            for (int c = 0; c < D / 64; ++c) {
+                tma_load_3d(sm.k[c], &a.tm_k, c * 64, g, k0, &sm.kv_full);
+                tma_load_3d(sm.v[c], &a.tm_v, c * 64, g, k0, &sm.kv_full);
+            }
+            int last_q[kQStages], last_do[kQStages];
+            for (int s = 0; s < kQStages; ++s) last_q[s] = last_do[s] = -1;
+            for (int i = 0; i < nsteps; ++i) {
+                const int st = i % kQStages, u = i / kQStages;
+                const int h = g * group + i / nq;
+                const int q0 = tl.seg_start + (tl.t + i % nq) * kTile;
+                if (u > 0 && !mbar_wait(&sm.q_empty[st], (u - 1) & 1, abort_flag, a.status)) break;
+                mbar_arrive_expect_tx(&sm.q_full[st], kTileBytes);
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q[st][c], &a.tm_q, c * 64, h, q0, &sm.q_full[st]);
+                last_q[st] = u;
+                if (u > 0 && !mbar_wait(&sm.do_empty[st], (u - 1) & 1, abort_flag, a.status)) break;
+                mbar_arrive_expect_tx(&sm.do_full[st], kTileBytes);
+                for (int c = 0; c < D / 64; ++c)
+                    tma_load_3d(sm.dout[st][c], &a.tm_do, c * 64, h, q0, &sm.do_full[st]);
+                last_do[st] = u;
+            }
+            if (*abort_flag) {
+                // Let the copies still in flight land before the CTA exits.
+                wait_drain(&sm.kv_full, 0);
+                for (int s = 0; s < kQStages; ++s) {
+                    if (last_q[s] >= 0) wait_drain(&sm.q_full[s], last_q[s] & 1);
+                    if (last_do[s] >= 0) wait_drain(&sm.do_full[s], last_do[s] & 1);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t id_ss = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
+            constexpr uint32_t id_kn = idesc_bf16(128, D, 0, 1);    // dV, dK
+            constexpr uint32_t id_mn = idesc_bf16(128, D, 1, 1);    // dQ
+            const uint32_t k_addr = smem_u32(sm.k[0]), v_addr = smem_u32(sm.v[0]);
+            const uint32_t pds_addr = smem_u32(sm.pds[0]);
+            int q_commits[kQStages] = {}, do_commits[kQStages] = {};
+            bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, a.status);
+            for (int i = 0; ok && i < nsteps; ++i) {
+                const int st = i % kQStages, u = i / kQStages;
+                const uint32_t q_addr = smem_u32(sm.q[st][0]), do_addr = smem_u32(sm.dout[st][0]);
+                const uint32_t ph = i & 1, pph = (i - 1) & 1;
+                // S^T = K Q^T  (M = kv, N = q, K = d)
+                if (!mbar_wait(&sm.q_full[st], u & 1, abort_flag, a.status)) { ok = false; break; }
+                if (i > 0 && !mbar_wait(&sm.dq_free, pph, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                    umma_bf16(tmem + 0, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
+                              id_ss, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&sm.s_full);
+                // dP^T = V dO^T
+                if (!mbar_wait(&sm.do_full[st], u & 1, abort_flag, a.status)) { ok = false; break; }
+                if (i > 0 && !mbar_wait(&sm.dp_free, pph, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                    umma_bf16(tmem + 128, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
+                              id_ss, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&sm.dp_full);
+                // dV += P^T dO  (M = kv, N = d, K = q)
+                if (!mbar_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 128 / 16; ++kk)
+                    umma_bf16(tmem + kDV, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                              sdesc_sw128(do_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&sm.dv_done);
+                umma_commit(&sm.do_empty[st]);
+                ++do_commits[st];
+                // dK += dS^T Q, dQ_part = dS K
+                if (!mbar_wait(&sm.ds_full, ph, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 128 / 16; ++kk)
+                    umma_bf16(tmem + kDK, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                              sdesc_sw128(q_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < 128 / 16; ++kk)
+                    umma_bf16(tmem + 0, sdesc_sw128(pds_addr + kk * 2048, kAtom, 1024),
+                              sdesc_sw128(k_addr + kk * 2048, kAtom, 1024), id_mn, kk > 0 ? 1u : 0u);
+                umma_commit(&sm.pds_free);
+                umma_commit(&sm.q_empty[st]);
+                ++q_commits[st];
+                umma_commit(&sm.dq_full);
+            }
+            umma_commit(&sm.fin);
+            umma_commit(&sm.drain);
+            wait_drain(&sm.drain, 0);
+            for (int s = 0; s < kQStages; ++s) {
+                if (q_commits[s] > 0) wait_drain(&sm.q_empty[s], (q_commits[s] - 1) & 1);
+                if (do_commits[s] > 0) wait_drain(&sm.do_empty[s], (do_commits[s] - 1) & 1);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ compute
+        const int t = threadIdx.x;  // kv row (and q row for dQ) = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t pds_addr = smem_u32(sm.pds[0]);
+        const float sl2 = a.scale_log2;
+        const int kj = k0 + t;
+        bool ok = true;
+        // prefetch the step's per-column terms
+        auto col_terms = [&](int i, float &l2, float &dd) {
+            const int h = g * group + i / nq;
+            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + t;
+            l2 = 0.f;
+            dd = 0.f;
+            if (qi < a.total_tokens) {
+                const size_t idx = static_cast<size_t>(h) * a.total_tokens + qi;
+                l2 = a.lse[idx] * 1.4426950408889634f;
+                dd = a.delta[idx];
+            }
+        };
+        float nl2, ndd;
+        col_terms(0, nl2, ndd);
+        for (int i = 0; i < nsteps; ++i) {
+            const int h = g * group + i / nq;
+            const int qt = tl.t + i % nq;
+            const int q0 = tl.seg_start + qt * kTile;
+            const uint32_t ph = i & 1, pph = (i - 1) & 1;
+            sm.lse2[i & 1][t] = nl2;
+            sm.delta[i & 1][t] = ndd;
+            mbar_arrive(&sm.cols[i & 1]);
+            if (i + 1 < nsteps) col_terms(i + 1, nl2, ndd);
+            if (!warp_wait(&sm.cols[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            const float *L2 = sm.lse2[i & 1];
+            const float *DD = sm.delta[i & 1];
+            // column c (q row q0 + c) is live for kv row kj iff kj <= q0 + c < seg_end
+            const int c_lo = kj - q0;                 // first live column
+            const int c_hi = tl.seg_end - q0;         // columns >= c_hi are past the segment
+
+            // P^T = exp(S^T * scale - LSE)
+            if (!warp_wait(&sm.s_full, ph, abort_flag, a.status)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                tmem_ld32(tmem + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                float p = ex2(__uint_as_float(s[c]) * sl2 - L2[c]);
+                if (c < c_lo || c >= c_hi) p = 0.f;
+                s[c] = __float_as_uint(p);
+            }
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+            if (i > 0 && !warp_wait(&sm.pds_free, pph, abort_flag, a.status)) { ok = false; break; }
+            store_row_sw128(pds_addr, t, pk);
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.p_full);
+
+            // dS^T = P^T * (dP^T - D)
+            if (!warp_wait(&sm.dp_full, ph, abort_flag, a.status)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t dp[32];
+                tmem_ld32(tmem + lane_off + 128 + c * 32, dp);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int c0 = c * 32 + 2 * e;
+                    float d0 = __uint_as_float(s[c0]) * (__uint_as_float(dp[2 * e]) - DD[c0]);
+                    float d1 = __uint_as_float(s[c0 + 1]) * (__uint_as_float(dp[2 * e + 1]) - DD[c0 + 1]);
+                    pk[c * 16 + e] = pack_bf16x2(d0, d1);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.dp_free);
+            if (!warp_wait(&sm.dv_done, ph, abort_flag, a.status)) { ok = false; break; }
+            store_row_sw128(pds_addr, t, pk);
+            fence_proxy_async_smem();
+            mbar_arrive(&sm.ds_full);
+
+            // dQ rows q0 + t: accumulate into HBM
+            if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
+            tc_fence_after();
+            const int qrow = q0 + t;
+            float *dst = a.dq_acc + (static_cast<size_t>(h) * a.total_tokens + qrow) * D;
+            const bool live = qrow < tl.seg_end;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + c * 32, v);
+                tmem_wait_ld();
+                if (live) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.dq_free);
+        }
+        // dK, dV rows of this tile
+        if (ok && warp_wait(&sm.fin, 0, abort_flag, a.status)) {
+            tc_fence_after();
+            const bool live = kj < tl.seg_end;
+            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + g) * D;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which ? kDK : kDV;
+                const float mul = which ? a.scale : 1.f;
+                void *base = which ? a.dk : a.dv;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + col + c * 32, v);
+                    tmem_wait_ld();
+                    if (!live) continue;
+                    if (a.grad_fp32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base) + orow + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                                                 __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + orow + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                                pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                                pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                                pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t stream)
+{
+    const int T = a.total_tokens;
+    const long long rows = static_cast<long long>(T) * a.Hq;
+    {
+        long long blocks = (rows * 8 + 255) / 256;
+        if (blocks > 152 * 16) blocks = 152 * 16;
+        if (blocks < 1) blocks = 1;
+        bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.out, a.dout, a.delta, a.dq_acc, T, a.Hq);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const size_t smem = sizeof(BwdSmem<D>);
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = grid_tiles * a.Hkv;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (grid > 0) {
+        attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    long long blocks = (rows * (D / 8) + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.dq_acc, a.dq, a.grad_fp32, a.scale, T, a.Hq);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const AttnBwdArgs &a, int head_dim, int64_t grid_tiles, cudaStream_t stream)
+{
+    if (head_dim == 64) return launch_bwd_d<64>(a, grid_tiles, stream);
+    if (head_dim == 128) return launch_bwd_d<128>(a, grid_tiles, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace spd

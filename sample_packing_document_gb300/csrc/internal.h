@@ -1,0 +1,111 @@
+// Launch functions shared between the C-ABI front end (api.cu) and the kernel
+// translation units. Host-side only; every function launches on `stream` and
+// returns a cudaError_t.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace spd {
+
+// Workspace header: [0] status word, [1] tile count; the rest per operation.
+constexpr size_t kWsHeader = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- packing
+struct PackArgs {
+    const int32_t *tokens;
+    const int32_t *doc_lens;
+    int32_t num_docs;
+    int32_t num_tokens;
+    int32_t micro_bsz;
+    int32_t seq_len;
+    int32_t plen;
+    int32_t rows;
+    int32_t packed;
+    int32_t *input_ids;
+    int32_t *labels;
+    int32_t *indexes;
+    int32_t *cu_seqlens;
+    int32_t *row_seg_ptr;
+    int32_t *max_seqlen;
+    int32_t *num_segs;
+    int *status;
+    // workspace arrays, num_docs + 1 entries each
+    int32_t *doc_out;   // first output position of each document (+ sentinel)
+    int32_t *doc_in;    // first input position of each document
+    int32_t *doc_keep;  // tokens kept of each document
+    int vec_out;        // 1: output pointers are 16-byte aligned
+    int vec_in;         // 1: tokens is 16-byte aligned
+};
+
+size_t pack_ws_bytes(int64_t num_docs);
+cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- tile schedule
+// One work tile: a 128-token block of one segment. Sorted by cost, largest
+// first. `cost` is the number of 128-blocks of the segment a tile touches in
+// the forward direction (tile t of a segment: t + 1).
+struct Tile {
+    int32_t seg_start;
+    int32_t seg_end;
+    int32_t t;      // block index inside the segment
+    int32_t cost;
+};
+
+constexpr int kTile = 128;
+
+// Upper bound of the tile count for total_tokens tokens in num_segs segments.
+inline int64_t max_tiles(int64_t total_tokens, int64_t num_segs)
+{
+    return (total_tokens + kTile - 1) / kTile + num_segs;
+}
+
+// Builds the work list into the workspace (after the header): validates
+// cu_seqlens (status SPD_ERR_BAD_SEQLENS on failure) and writes the tile count
+// to ws[1]. order: 0 = forward costs (t + 1), 1 = backward costs (n - t).
+cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
+                            int order, void *ws, cudaStream_t stream);
+size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs);
+
+// ---------------------------------------------------------------- attention
+struct AttnFwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v;
+    uint16_t *out;
+    float *lse;
+    const Tile *tiles;
+    const int32_t *tile_count;
+    int *status;
+    int32_t total_tokens;
+    int32_t Hq, Hkv;
+    float scale_log2;  // softmax_scale * log2(e)
+    float scale;
+};
+
+cudaError_t launch_attn_fwd(const AttnFwdArgs &a, int head_dim, int64_t grid_tiles,
+                            cudaStream_t stream);
+
+struct AttnBwdArgs {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    const uint16_t *out;
+    const uint16_t *dout;
+    const float *lse;
+    float *dq_acc;   // [Hq, total_tokens, head_dim] fp32
+    float *delta;    // [Hq, total_tokens] fp32
+    void *dq, *dk, *dv;
+    int grad_fp32;
+    const Tile *tiles;
+    const int32_t *tile_count;
+    int *status;
+    int32_t total_tokens;
+    int32_t Hq, Hkv;
+    float scale_log2;
+    float scale;
+};
+
+cudaError_t launch_attn_bwd(const AttnBwdArgs &a, int head_dim, int64_t grid_tiles,
+                            cudaStream_t stream);
+
+}  // namespace spd

@@ -1,0 +1,366 @@
+// Packing kernels: documents -> packed rows (input_ids, labels, indexes) and
+// the segment fields (cu_seqlens, row_seg_ptr, max_seqlen, num_segs).
+//
+// Rules: InternEvo page "Data loading and flow", section "Dataloader loading
+// data" (build_pack with use_packed_dataset = True, build_unpack with False;
+// pad id 0, label = next token of the same document, -100 at a document's last
+// token and on padding) and section "Fetching data from the Dataloader"
+// (cu_seqlens: segment boundaries of a row, the padding tail being its own
+// segment; indexes: position inside the current segment).
+//
+// Two launches on one stream:
+//   pack_scan_kernel    one CTA: prefix sums over the document lengths, the
+//                       document -> output position map, cu_seqlens,
+//                       row_seg_ptr, max_seqlen, num_segs. Work ~ num_docs.
+//   pack_stream_kernel  all SMs: the token stream, 16-byte vector stores of
+//                       input_ids / labels / indexes. Work ~ output positions.
+// The stream kernel is a programmatic dependent launch: in build_pack mode it
+// copies input_ids (which needs no document boundaries) while the scan runs,
+// then waits for the scan's results before labels and indexes.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace spd {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 4;  // documents per thread per pass
+constexpr int kStreamThreads = 256;
+constexpr int kStreamIters = 4;
+constexpr int kChunk = kStreamThreads * 4 * kStreamIters;  // positions per CTA
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+// Returns the exclusive prefix; *total gets the block sum. `sh` holds 33 slots.
+__device__ long long block_excl_scan(long long v, long long *total, long long *sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = sh[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        sh[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    long long warp_excl = warp ? sh[warp - 1] : 0;
+    *total = sh[31];
+    __syncthreads();  // sh is reused by the next call
+    return warp_excl + x - v;
+}
+
+// First index d in [lo, hi) with a[d] >= x (hi if none); a strictly increasing.
+__device__ __forceinline__ int lower_bound(const int32_t *a, int lo, int hi, long long x)
+{
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (a[mid] < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Largest d in [lo, hi) with a[d] <= x; assumes a[lo] <= x.
+__device__ __forceinline__ int last_le(const int32_t *a, int lo, int hi, long long x)
+{
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (a[mid] <= x) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kScanThreads) pack_scan_kernel(PackArgs a, int32_t *aux)
+{
+    pdl_launch_dependents();
+    __shared__ long long sh[33];
+    __shared__ int bad_s;
+    const int tid = threadIdx.x;
+    const int nd = a.num_docs;
+    const long long plen = a.plen;
+    if (tid == 0) {
+        *a.status = 0;
+        bad_s = 0;
+    }
+    for (int r = tid; r < a.rows; r += kScanThreads) a.max_seqlen[r] = 0;
+
+    // Pass 1: exclusive prefix sums of the raw lengths (input offsets) and of
+    // the kept lengths (output offsets before the row split).
+    long long carry_raw = 0, carry_keep = 0;
+    bool bad = false;
+    for (int base = 0; base < nd; base += kScanThreads * kScanItems) {
+        int len[kScanItems], keep[kScanItems];
+        long long sraw = 0, skeep = 0;
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            int d = base + tid * kScanItems + k;
+            len[k] = d < nd ? a.doc_lens[d] : 0;
+            if (d < nd && len[k] <= 0) bad = true;
+            if (len[k] < 0) len[k] = 0;
+            keep[k] = a.packed ? len[k] : min(len[k], a.seq_len);
+            sraw += len[k];
+            skeep += keep[k];
+        }
+        long long traw, tkeep;
+        long long eraw = block_excl_scan(sraw, &traw, sh) + carry_raw;
+        long long ekeep = block_excl_scan(skeep, &tkeep, sh) + carry_keep;
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            int d = base + tid * kScanItems + k;
+            if (d < nd) {
+                a.doc_in[d] = static_cast<int32_t>(eraw);
+                a.doc_keep[d] = keep[k];
+                aux[d] = static_cast<int32_t>(ekeep);  // unpack: global kept prefix
+            }
+            eraw += len[k];
+            ekeep += keep[k];
+        }
+        carry_raw += traw;
+        carry_keep += tkeep;
+        if (carry_raw > 0x7fffffffLL) bad = true;
+    }
+    if (bad) atomicOr(&bad_s, 1);
+    __syncthreads();
+    if (bad_s || carry_raw != a.num_tokens) {
+        if (tid == 0) {
+            set_status(a.status, kErrBadDocs);
+            *a.num_segs = 0;
+        }
+        return;
+    }
+    if (tid == 0) {
+        a.doc_in[nd] = static_cast<int32_t>(carry_raw);
+        aux[nd] = static_cast<int32_t>(carry_keep);
+    }
+    __syncthreads();
+
+    int num_segs;
+    if (a.packed) {
+        // Segment boundaries are the union of document starts, row starts and
+        // the padding start. A document start that falls on a row start is
+        // the same boundary; count those ("aligned") so ranks stay exact.
+        long long carry_al = 0;
+        for (int base = 0; base < nd; base += kScanThreads) {
+            int d = base + tid;
+            int flag = (d >= 1 && d < nd && (a.doc_in[d] % plen) == 0) ? 1 : 0;
+            long long tot;
+            long long e = block_excl_scan(flag, &tot, sh) + carry_al;
+            if (d < nd) aux[d] = static_cast<int32_t>(e);  // aligned starts before d
+            carry_al += tot;
+        }
+        if (tid == 0) aux[nd] = static_cast<int32_t>(carry_al);
+        __syncthreads();
+        const long long total = a.num_tokens;
+        const int pad = (total % plen) != 0;
+        num_segs = a.rows == 0 ? 0 : static_cast<int>(a.rows + nd - 1 - aux[nd] + pad);
+        for (int d = tid; d < nd; d += kScanThreads) {
+            long long s = a.doc_in[d];
+            a.doc_out[d] = static_cast<int32_t>(s);
+            if (d >= 1 && (s % plen) != 0) {
+                long long rank = (s - 1) / plen + d - aux[d];
+                a.cu_seqlens[rank] = static_cast<int32_t>(s);
+            }
+        }
+        if (tid == 0) a.doc_out[nd] = static_cast<int32_t>(total);
+        for (int r = tid; r <= a.rows; r += kScanThreads) {
+            long long rank = 0;
+            if (r > 0) {
+                int ds = lower_bound(a.doc_in, 0, nd, r * plen);
+                rank = r + ds - 1 - aux[ds] + ((r == a.rows && pad) ? 1 : 0);
+            }
+            a.cu_seqlens[rank] = static_cast<int32_t>(r * plen);
+            a.row_seg_ptr[r] = static_cast<int32_t>(rank);
+        }
+        if (tid == 0 && pad) a.cu_seqlens[num_segs - 1] = static_cast<int32_t>(total);
+    } else {
+        // One segment per kept document, plus a padding segment in every row
+        // that the kept documents do not fill.
+        const int mb = a.micro_bsz;
+        long long carry_pad = 0;
+        for (int base = 0; base < a.rows; base += kScanThreads) {
+            int r = base + tid;
+            int flag = 0;
+            if (r < a.rows) {
+                int d0 = r * mb, d1 = min(nd, d0 + mb);
+                long long fill = static_cast<long long>(aux[d1]) - aux[d0];
+                flag = fill < plen ? 1 : 0;
+            }
+            long long tot;
+            long long e = block_excl_scan(flag, &tot, sh) + carry_pad;
+            if (r < a.rows) a.row_seg_ptr[r] = static_cast<int32_t>(static_cast<long long>(r) * mb + e);
+            carry_pad += tot;
+        }
+        num_segs = static_cast<int>(nd + carry_pad);
+        if (tid == 0) a.row_seg_ptr[a.rows] = num_segs;
+        __syncthreads();
+        for (int d = tid; d < nd; d += kScanThreads) {
+            int r = d / mb;
+            long long out = r * plen + aux[d] - aux[r * mb];
+            a.doc_out[d] = static_cast<int32_t>(out);
+            a.cu_seqlens[a.row_seg_ptr[r] + (d - r * mb)] = static_cast<int32_t>(out);
+        }
+        for (int r = tid; r < a.rows; r += kScanThreads) {
+            int d0 = r * mb, d1 = min(nd, d0 + mb);
+            long long fill = static_cast<long long>(aux[d1]) - aux[d0];
+            if (fill < plen)
+                a.cu_seqlens[a.row_seg_ptr[r] + (d1 - d0)] = static_cast<int32_t>(r * plen + fill);
+        }
+        if (tid == 0) a.cu_seqlens[num_segs] = static_cast<int32_t>(a.rows * plen);
+    }
+    if (tid == 0) *a.num_segs = num_segs;
+    __syncthreads();
+    for (int i = tid; i < num_segs; i += kScanThreads) {
+        int s = a.cu_seqlens[i];
+        atomicMax(&a.max_seqlen[s / plen], a.cu_seqlens[i + 1] - s);
+    }
+}
+
+// Per output position: id, label, index. `d_hint` is a document index at or
+// before the one holding p (build_pack) and is advanced in place.
+template <bool kPacked>
+__device__ __forceinline__ void one_position(const PackArgs &a, long long p, int &d, int d_end,
+                                             int32_t &id, int32_t &lab, int32_t &idx)
+{
+    const long long plen = a.plen;
+    if (kPacked) {
+        const long long total = a.num_tokens;
+        if (p >= total) {
+            id = 0;
+            lab = -100;
+            idx = static_cast<int32_t>(p - total);
+            return;
+        }
+        while (d + 1 < d_end && a.doc_out[d + 1] <= p) ++d;
+        const long long start = a.doc_out[d], end = a.doc_out[d + 1];
+        id = a.tokens[p];
+        lab = (p + 1 < end) ? a.tokens[p + 1] : -100;
+        const long long row_start = (p / plen) * plen;
+        idx = static_cast<int32_t>(p - (start > row_start ? start : row_start));
+    } else {
+        const long long r = p / plen;
+        const int d0 = static_cast<int>(r * a.micro_bsz);
+        const int d1 = min(a.num_docs, d0 + a.micro_bsz);
+        const int dd = last_le(a.doc_out, d0, d1, p);
+        const long long start = a.doc_out[dd];
+        const int keep = a.doc_keep[dd];
+        const long long t = p - start;
+        if (t < keep) {
+            const long long src = static_cast<long long>(a.doc_in[dd]) + t;
+            id = a.tokens[src];
+            lab = (t + 1 < keep) ? a.tokens[src + 1] : -100;
+            idx = static_cast<int32_t>(t);
+        } else {
+            id = 0;
+            lab = -100;
+            idx = static_cast<int32_t>(t - keep);
+        }
+    }
+}
+
+template <bool kPacked>
+__global__ void __launch_bounds__(kStreamThreads) pack_stream_kernel(PackArgs a)
+{
+    const long long npos = static_cast<long long>(a.rows) * a.plen;
+    const long long P0 = static_cast<long long>(blockIdx.x) * kChunk;
+    const long long P1 = min(npos, P0 + kChunk);
+
+    if (kPacked) {
+        // input_ids needs no document boundaries: copy it while the scan runs.
+        for (int it = 0; it < kStreamIters; ++it) {
+            long long p = P0 + (static_cast<long long>(it) * kStreamThreads + threadIdx.x) * 4;
+            if (p >= P1) break;
+            if (a.vec_out && a.vec_in && p + 4 <= a.num_tokens) {
+                *reinterpret_cast<int4 *>(a.input_ids + p) =
+                    *reinterpret_cast<const int4 *>(a.tokens + p);
+            } else {
+                for (int k = 0; k < 4 && p + k < P1; ++k)
+                    a.input_ids[p + k] = p + k < a.num_tokens ? a.tokens[p + k] : 0;
+            }
+        }
+    }
+    pdl_wait();
+    if (*reinterpret_cast<volatile int *>(a.status) != 0) return;
+
+    __shared__ int d_lo_s, d_hi_s;
+    if (kPacked) {
+        if (threadIdx.x == 0) {
+            long long last_tok = a.num_tokens - 1;
+            long long q0 = P0 < last_tok ? P0 : last_tok;
+            long long q1 = (P1 - 1) < last_tok ? (P1 - 1) : last_tok;
+            d_lo_s = a.num_docs > 0 ? last_le(a.doc_out, 0, a.num_docs, q0) : 0;
+            d_hi_s = a.num_docs > 0 ? last_le(a.doc_out, 0, a.num_docs, q1) + 1 : 0;
+        }
+        __syncthreads();
+    }
+    for (int it = 0; it < kStreamIters; ++it) {
+        long long p = P0 + (static_cast<long long>(it) * kStreamThreads + threadIdx.x) * 4;
+        if (p >= P1) break;
+        int d = 0;
+        if (kPacked && p < a.num_tokens) d = last_le(a.doc_out, d_lo_s, d_hi_s, p);
+        int32_t id[4], lab[4], idx[4];
+        const int n = static_cast<int>(min(4LL, P1 - p));
+        for (int k = 0; k < n; ++k)
+            one_position<kPacked>(a, p + k, d, d_hi_s, id[k], lab[k], idx[k]);
+        if (a.vec_out && n == 4) {
+            if (!kPacked) *reinterpret_cast<int4 *>(a.input_ids + p) = make_int4(id[0], id[1], id[2], id[3]);
+            *reinterpret_cast<int4 *>(a.labels + p) = make_int4(lab[0], lab[1], lab[2], lab[3]);
+            *reinterpret_cast<int4 *>(a.indexes + p) = make_int4(idx[0], idx[1], idx[2], idx[3]);
+        } else {
+            for (int k = 0; k < n; ++k) {
+                if (!kPacked) a.input_ids[p + k] = id[k];
+                a.labels[p + k] = lab[k];
+                a.indexes[p + k] = idx[k];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+size_t pack_ws_bytes(int64_t num_docs)
+{
+    // status header + 4 arrays of num_docs + 1 int32
+    return kWsHeader + 4 * align_up(sizeof(int32_t) * static_cast<size_t>(num_docs + 1), 256);
+}
+
+cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
+{
+    (void)num_sms;
+    PackArgs a = a_in;
+    const size_t arr = align_up(sizeof(int32_t) * static_cast<size_t>(a.num_docs + 1), 256);
+    char *ws = reinterpret_cast<char *>(a.status);
+    a.doc_out = reinterpret_cast<int32_t *>(ws + kWsHeader);
+    a.doc_in = reinterpret_cast<int32_t *>(ws + kWsHeader + arr);
+    a.doc_keep = reinterpret_cast<int32_t *>(ws + kWsHeader + 2 * arr);
+    int32_t *aux = reinterpret_cast<int32_t *>(ws + kWsHeader + 3 * arr);
+
+    pack_scan_kernel<<<1, kScanThreads, 0, stream>>>(a, aux);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    const long long npos = static_cast<long long>(a.rows) * a.plen;
+    if (npos == 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((npos + kChunk - 1) / kChunk));
+    cfg.blockDim = dim3(kStreamThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.packed) return cudaLaunchKernelEx(&cfg, pack_stream_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, pack_stream_kernel<false>, a);
+}
+
+}  // namespace spd

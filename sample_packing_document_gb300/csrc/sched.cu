@@ -1,0 +1,160 @@
+// Tile scheduler: cu_seqlens -> a work list of 128-token tiles, longest first.
+//
+// Varlen attention splits the block-diagonal causal mask into one causal
+// attention per document (page "Sample Packing: attention problems of
+// long-sequence LLM training", section 5.1 "FlashAttention"), so a tile never
+// spans two segments and only the tiles of each document's own causal
+// triangle are ever visited. In the forward pass, q tile t of a segment reads
+// kv tiles 0..t (cost t + 1); in the backward pass, kv tile t reads q tiles
+// t..n-1 of its segment (cost n - t). Listing tiles by decreasing cost
+// (longest-processing-time first) lets the many short tiles fill in behind
+// the few long ones when documents are very uneven.
+//
+// One CTA: validates cu_seqlens, counts tiles per segment (exclusive scan ->
+// tile offsets), then a counting sort by cost over all tiles in parallel.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace spd {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kCostCap = 4095;  // costs above this share one bin (order among them is free)
+
+__device__ long long block_scan_excl(long long v, long long *total, long long *sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = sh[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            long long y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        sh[lane] = w;
+    }
+    __syncthreads();
+    long long r = (warp ? sh[warp - 1] : 0) + x - v;
+    *total = sh[31];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, int32_t nsegs,
+                                                            int64_t T, int order, int *status,
+                                                            int32_t *count, Tile *tiles,
+                                                            int32_t *tile_off)
+{
+    __shared__ int bins[kCostCap + 1];
+    __shared__ long long sh[33];
+    __shared__ int bad_s;
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        *status = 0;
+        bad_s = 0;
+    }
+    for (int c = tid; c <= kCostCap; c += kThreads) bins[c] = 0;
+    __syncthreads();
+
+    // Validate and count tiles per segment.
+    bool bad = (tid == 0) && (cu[0] != 0 || static_cast<int64_t>(cu[nsegs]) != T);
+    long long carry = 0;
+    for (int base = 0; base < nsegs; base += kThreads) {
+        int s = base + tid;
+        long long n = 0;
+        if (s < nsegs) {
+            int a = cu[s], b = cu[s + 1];
+            if (b <= a) bad = true;
+            else n = (b - a + kTile - 1) / kTile;
+        }
+        long long tot;
+        long long e = block_scan_excl(n, &tot, sh) + carry;
+        if (s < nsegs) tile_off[s] = static_cast<int32_t>(e);
+        carry += tot;
+    }
+    if (bad) atomicOr(&bad_s, 1);
+    if (tid == 0) tile_off[nsegs] = static_cast<int32_t>(carry);
+    __syncthreads();
+    if (bad_s) {
+        if (tid == 0) {
+            set_status(status, kErrBadSeqlens);
+            *count = 0;
+        }
+        return;
+    }
+    const int ntiles = static_cast<int>(carry);
+
+    auto locate = [&](int i, int &s, int &t, int &n, int &cost) {
+        int lo = 0, hi = nsegs;  // largest s with tile_off[s] <= i
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (tile_off[mid] <= i) lo = mid;
+            else hi = mid;
+        }
+        s = lo;
+        t = i - tile_off[s];
+        n = tile_off[s + 1] - tile_off[s];
+        cost = order ? n - t : t + 1;
+    };
+
+    for (int i = tid; i < ntiles; i += kThreads) {
+        int s, t, n, cost;
+        locate(i, s, t, n, cost);
+        atomicAdd(&bins[min(cost, kCostCap)], 1);
+    }
+    __syncthreads();
+    // Descending exclusive scan: bins[c] <- number of tiles with a larger cost.
+    if (tid == 0) {
+        int run = 0;
+        for (int c = kCostCap; c >= 0; --c) {
+            int v = bins[c];
+            bins[c] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < ntiles; i += kThreads) {
+        int s, t, n, cost;
+        locate(i, s, t, n, cost);
+        int pos = atomicAdd(&bins[min(cost, kCostCap)], 1);
+        Tile w;
+        w.seg_start = cu[s];
+        w.seg_end = cu[s + 1];
+        w.t = t;
+        w.cost = cost;
+        tiles[pos] = w;
+    }
+    if (tid == 0) *count = ntiles;
+}
+
+}  // namespace
+
+size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs)
+{
+    return kWsHeader + align_up(sizeof(Tile) * static_cast<size_t>(max_tiles(total_tokens, num_segs)), 256) +
+           align_up(sizeof(int32_t) * static_cast<size_t>(num_segs + 1), 256);
+}
+
+cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
+                            int order, void *ws, cudaStream_t stream)
+{
+    char *base = reinterpret_cast<char *>(ws);
+    int *status = reinterpret_cast<int *>(base);
+    int32_t *count = reinterpret_cast<int32_t *>(base) + 1;
+    Tile *tiles = reinterpret_cast<Tile *>(base + kWsHeader);
+    int32_t *tile_off = reinterpret_cast<int32_t *>(
+        base + kWsHeader + align_up(sizeof(Tile) * static_cast<size_t>(max_tiles(total_tokens, num_segs)), 256));
+    schedule_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_segs, total_tokens, order, status,
+                                                count, tiles, tile_off);
+    return cudaGetLastError();
+}
+
+}  // namespace spd

@@ -1,0 +1,203 @@
+"""Python binding of libspd.so: argument marshalling only.
+
+Every step runs in the library's CUDA kernels; torch supplies device memory
+and the current stream. There is no CPU fallback: if the library or a GB300
+is missing, the first call raises.
+
+Names follow the C ABI in include/spd.h.
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libspd.so")
+_lib = None
+
+SPD_OK = 0
+_P = ctypes.c_void_p
+_I32, _I64, _INT, _F32, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+# name -> (restype, argtypes); the full exported surface of include/spd.h
+SIGNATURES = {
+    "spd_status_string": (ctypes.c_char_p, [_INT]),
+    "spd_version": (_INT, []),
+    "spd_read_status": (_INT, [_P, _P, ctypes.POINTER(_INT)]),
+    "spd_pack_rows": (_INT, [_I64, _I64, _INT, _INT, _INT, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "spd_pack_workspace_size": (_SZ, [_I64]),
+    "spd_pack_tokens": (_INT, [_P, _P, _I64, _I64, _INT, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "spd_attn_workspace_size": (_SZ, [_I64, _I32, _INT, _INT, _INT, _INT]),
+    "spd_varlen_attn_fwd": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _P, _P, _P, _SZ, _P]),
+    "spd_varlen_attn_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _INT,
+                                   _P, _P, _P, _P, _SZ, _P]),
+}
+
+
+class SpdError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (fn, status_string(status), status))
+
+
+def load(path=_LIB_PATH):
+    """Load libspd.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError("libspd.so is not built (run __graft_entry__.build()); there is no CPU fallback")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def status_string(status):
+    return load().spd_status_string(int(status)).decode()
+
+
+def _check(fn, rc):
+    if rc != SPD_OK:
+        raise SpdError(fn, rc)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need_cuda(*ts):
+    if not torch.cuda.is_available():
+        raise RuntimeError("spd needs a CUDA GPU (GB300); there is no CPU fallback")
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("inputs must be contiguous CUDA tensors")
+
+
+def workspace(nbytes, device=None):
+    """A 256-byte aligned byte buffer (torch allocations are)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def read_status(ws, stream=None):
+    """Synchronise and return the device status word of the last call on ws."""
+    v = _INT(0)
+    _check("spd_read_status", load().spd_read_status(_ptr(ws), _stream(stream), ctypes.byref(v)))
+    return v.value
+
+
+# ----------------------------------------------------------------------------- packing
+
+def pack_rows(num_docs, num_tokens, micro_bsz, seq_len, use_packed_dataset=True):
+    rows, max_segs = _I64(0), _I64(0)
+    _check("spd_pack_rows", load().spd_pack_rows(int(num_docs), int(num_tokens), int(micro_bsz), int(seq_len),
+                                                 int(bool(use_packed_dataset)), ctypes.byref(rows),
+                                                 ctypes.byref(max_segs)))
+    return rows.value, max_segs.value
+
+
+def pack_workspace_size(num_docs):
+    return load().spd_pack_workspace_size(int(num_docs))
+
+
+def alloc_pack_outputs(num_docs, num_tokens, micro_bsz, seq_len, use_packed_dataset=True, device="cuda"):
+    rows, max_segs = pack_rows(num_docs, num_tokens, micro_bsz, seq_len, use_packed_dataset)
+    n = rows * micro_bsz * seq_len
+    i32 = dict(dtype=torch.int32, device=device)
+    return {
+        "rows": rows, "max_segs": max_segs,
+        "input_ids": torch.empty(n, **i32), "labels": torch.empty(n, **i32), "indexes": torch.empty(n, **i32),
+        "cu_seqlens": torch.empty(max_segs + 1, **i32), "row_seg_ptr": torch.empty(rows + 1, **i32),
+        "max_seqlen": torch.empty(max(rows, 1), **i32), "num_segs": torch.empty(1, **i32),
+        "ws": workspace(pack_workspace_size(num_docs), device),
+    }
+
+
+def pack_tokens(tokens, doc_lens, micro_bsz, seq_len, use_packed_dataset=True, out=None, stream=None):
+    """spd_pack_tokens. tokens / doc_lens: int32 CUDA tensors. Returns the
+    output dict (see alloc_pack_outputs); its num_segs stays on the device."""
+    _need_cuda(tokens, doc_lens)
+    assert tokens.dtype == torch.int32 and doc_lens.dtype == torch.int32
+    nd, nt = doc_lens.numel(), tokens.numel()
+    if out is None:
+        out = alloc_pack_outputs(nd, nt, micro_bsz, seq_len, use_packed_dataset, tokens.device)
+    ws = out["ws"]
+    _check("spd_pack_tokens", load().spd_pack_tokens(
+        _ptr(tokens), _ptr(doc_lens), nd, nt, int(micro_bsz), int(seq_len), int(bool(use_packed_dataset)),
+        _ptr(out["input_ids"]), _ptr(out["labels"]), _ptr(out["indexes"]), _ptr(out["cu_seqlens"]),
+        _ptr(out["row_seg_ptr"]), _ptr(out["max_seqlen"]), _ptr(out["num_segs"]), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------------------- attention
+
+def attn_workspace_size(total_tokens, num_segs, Hq, Hkv, head_dim, bwd):
+    n = load().spd_attn_workspace_size(int(total_tokens), int(num_segs), int(Hq), int(Hkv), int(head_dim),
+                                       int(bool(bwd)))
+    if n == 0:
+        raise ValueError("unsupported attention shape")
+    return n
+
+
+def _as_u16(t):
+    assert t.dtype == torch.bfloat16
+    return t
+
+
+def varlen_attn_fwd(q, k, v, cu_seqlens, num_segs, max_seqlen=0, softmax_scale=None, out=None, lse=None,
+                    ws=None, stream=None):
+    """spd_varlen_attn_fwd. q [T, Hq, d], k / v [T, Hkv, d] bf16 CUDA tensors,
+    cu_seqlens int32 [num_segs + 1] CUDA tensor, num_segs a host int.
+    Returns (out bf16 [T, Hq, d], lse fp32 [Hq, T])."""
+    _need_cuda(q, k, v, cu_seqlens)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, T, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(attn_workspace_size(T, num_segs, Hq, Hkv, d, False), q.device)
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check("spd_varlen_attn_fwd", load().spd_varlen_attn_fwd(
+        _ptr(_as_u16(q)), _ptr(_as_u16(k)), _ptr(_as_u16(v)), _ptr(cu_seqlens), int(num_segs), T, int(max_seqlen),
+        Hq, Hkv, d, scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+    return out, lse
+
+
+def varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, num_segs, max_seqlen=0, softmax_scale=None,
+                    grad_dtype=torch.bfloat16, dq=None, dk=None, dv=None, ws=None, stream=None):
+    """spd_varlen_attn_bwd. Returns (dq, dk, dv) in grad_dtype (bf16 or fp32)."""
+    _need_cuda(q, k, v, out, dout, lse, cu_seqlens)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    assert grad_dtype in (torch.bfloat16, torch.float32)
+    if dq is None:
+        dq = torch.empty(T, Hq, d, dtype=grad_dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty(T, Hkv, d, dtype=grad_dtype, device=q.device)
+    if dv is None:
+        dv = torch.empty(T, Hkv, d, dtype=grad_dtype, device=q.device)
+    if ws is None:
+        ws = workspace(attn_workspace_size(T, num_segs, Hq, Hkv, d, True), q.device)
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check("spd_varlen_attn_bwd", load().spd_varlen_attn_bwd(
+        _ptr(_as_u16(q)), _ptr(_as_u16(k)), _ptr(_as_u16(v)), _ptr(_as_u16(out)), _ptr(_as_u16(dout)), _ptr(lse),
+        _ptr(cu_seqlens), int(num_segs), T, int(max_seqlen), Hq, Hkv, d, scale,
+        1 if grad_dtype == torch.float32 else 0, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return dq, dk, dv
+
+
+def default_scale(head_dim):
+    return 1.0 / math.sqrt(head_dim)

@@ -1,0 +1,83 @@
+"""The C-ABI library builds, loads and exports every entry point include/spd.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sample_packing_document_gb300 import build, ops
+    build.build()
+    return ops.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "spd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from sample_packing_document_gb300 import ops
+    names = _declared()
+    assert "spd_pack_tokens" in names and "spd_varlen_attn_fwd" in names and "spd_varlen_attn_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(ops.SIGNATURES)
+
+
+def test_status_strings_and_version(lib):
+    from sample_packing_document_gb300 import ops
+    assert lib.spd_version() >= 100
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert ops.status_string(code) != "unknown status"
+
+
+def test_pack_rows_host_logic(lib):
+    from sample_packing_document_gb300 import ops
+    assert ops.pack_rows(4, 24, 2, 8, True) == (2, 8)        # the page's example: 2 rows
+    assert ops.pack_rows(6, 44, 2, 8, False) == (3, 12)      # build_unpack example: 3 rows
+    assert ops.pack_rows(0, 0, 2, 8, True) == (0, 0)
+    with pytest.raises(ops.SpdError):
+        ops.pack_rows(1, 1, 0, 8, True)
+    with pytest.raises(ops.SpdError):
+        ops.pack_rows(1, 2 ** 31, 1, 8, True)
+    with pytest.raises(ops.SpdError):
+        ops.pack_rows(1, 0, 1, 8, True)
+
+
+def test_attn_workspace_and_rejections_without_gpu(lib):
+    from sample_packing_document_gb300 import ops
+    assert ops.attn_workspace_size(1000, 3, 4, 2, 128, False) > 0
+    bwd = ops.attn_workspace_size(1000, 3, 4, 2, 128, True)
+    assert bwd >= 4 * 1000 * 128 * 4                         # holds the fp32 dQ accumulator
+    assert lib.spd_attn_workspace_size(1000, 3, 4, 2, 96, 0) == 0    # head_dim 96 unsupported
+    assert lib.spd_attn_workspace_size(1000, 3, 6, 4, 128, 0) == 0   # Hq % Hkv != 0
+    # host checks come before any CUDA call
+    rc = lib.spd_varlen_attn_fwd(None, None, None, None, 3, 1000, 0, 4, 2, 96, 0.0, None, None, None, 0, None)
+    assert rc == -2
+    rc = lib.spd_varlen_attn_fwd(None, None, None, None, 3, 1000, 0, 4, 2, 128, 0.0, None, None, None, 0, None)
+    assert rc == -6
+    rc = lib.spd_varlen_attn_fwd(None, None, None, None, 0, 1000, 0, 4, 2, 128, 0.0, None, None, None, 0, None)
+    assert rc == -1
+    rc = lib.spd_varlen_attn_bwd(None, None, None, None, None, None, None, 3, 1000, 0, 4, 2, 128, 0.0, 2,
+                                 None, None, None, None, 0, None)
+    assert rc == -1
+    rc = lib.spd_pack_tokens(None, None, 2, 5, 2, 8, 1, None, None, None, None, None, None, None, None, 0, None)
+    assert rc == -6
+
+
+def test_oracle_does_not_leak_into_product():
+    """The product package never imports the oracle."""
+    pkg = os.path.join(ROOT, "sample_packing_document_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f
+                assert "oracle/" not in text and "liboracle" not in text, f

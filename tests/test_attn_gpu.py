@@ -1,0 +1,207 @@
+"""GPU parity of spd_varlen_attn_fwd / spd_varlen_attn_bwd against the fp64
+oracle on the same bf16 inputs.
+
+Bars (stated for this library): max |O - O_ref| <= 2e-2, max |LSE - LSE_ref|
+<= 1e-3, and max |g - g_ref| <= 5e-2 for dQ, dK, dV written as fp32. When the
+gradients are written as bf16 the rounding of the output itself (at most half
+a bf16 ulp, 2^-8 |g|) is added to the gradient bar.
+
+Small cases (several tiles, ragged tails, every segment-length class around
+the 128-token tile, GQA groups 1 / 2 / 3 / 7, head_dim 64 and 128) are
+compared element by element over all outputs. The five workloads at full size
+are compared on sampled rows (forward and dQ: any segment, including the
+longest; dK / dV: whole short segments) plus finiteness everywhere.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from oracle import pack as P
+
+pytestmark = pytest.mark.gpu
+
+TOL_O, TOL_LSE, TOL_G = 2e-2, 1e-3, 5e-2
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from sample_packing_document_gb300 import build, ops as _ops
+    build.build()
+    _ops.load()
+    return _ops
+
+
+def _u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _inputs(T, Hq, Hkv, d, seed, q_scale=1.0, device="cuda"):
+    from sample_packing_document_gb300 import workloads as W
+    return W.qkv(T, Hq, Hkv, d, seed, device=device, q_scale=q_scale)
+
+
+def _run(ops, q, k, v, do, cu, scale=None, grad_dtype=torch.float32):
+    cu_t = torch.tensor(np.asarray(cu, np.int32), device="cuda")
+    ns = len(cu) - 1
+    ws_f = ops.workspace(ops.attn_workspace_size(q.shape[0], ns, q.shape[1], k.shape[1], q.shape[2], False))
+    out, lse = ops.varlen_attn_fwd(q, k, v, cu_t, ns, softmax_scale=scale, ws=ws_f)
+    assert ops.read_status(ws_f) == 0
+    ws_b = ops.workspace(ops.attn_workspace_size(q.shape[0], ns, q.shape[1], k.shape[1], q.shape[2], True))
+    dq, dk, dv = ops.varlen_attn_bwd(q, k, v, out, do, lse, cu_t, ns, softmax_scale=scale, grad_dtype=grad_dtype,
+                                     ws=ws_b)
+    assert ops.read_status(ws_b) == 0
+    torch.cuda.synchronize()
+    return out, lse, dq, dk, dv
+
+
+def _maxerr(a, b):
+    return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64)))) if np.size(a) else 0.0
+
+
+def _check_full(ops, lens, Hq, Hkv, d, seed, scale=None, grad_dtype=torch.float32, q_scale=1.0):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v, do = _inputs(T, Hq, Hkv, d, seed, q_scale=q_scale)
+    out, lse, dq, dk, dv = _run(ops, q, k, v, do, cu, scale, grad_dtype)
+    qn, kn, vn, don = _u16(q), _u16(k), _u16(v), _u16(do)
+    o_ref, lse_ref = OA.attn_fwd(qn, kn, vn, cu, scale=scale)
+    o_gpu = out.float().cpu().numpy().transpose(1, 0, 2)
+    assert _maxerr(o_gpu, o_ref) <= TOL_O
+    assert _maxerr(lse.cpu().numpy(), lse_ref) <= TOL_LSE
+    gq, gk, gv, _ = OA.attn_bwd(qn, kn, vn, don, cu, scale=scale)
+    for g, ref in ((dq, gq), (dk, gk), (dv, gv)):
+        gn = g.float().cpu().numpy()
+        tol = TOL_G + (np.abs(ref) * 2.0 ** -8 if grad_dtype == torch.bfloat16 else 0.0)
+        assert np.all(np.abs(gn - ref) <= tol), _maxerr(gn, ref)
+    return out, lse, dq, dk, dv, (qn, kn, vn, don, cu)
+
+
+@pytest.mark.parametrize("lens,Hq,Hkv,d", [
+    ([3, 4, 5, 4], 2, 2, 64),                       # the page's documents 3, 4, 5, 4
+    ([300, 1, 129, 517, 2, 128, 1000], 4, 2, 128),  # tiles, ragged tails, 1 / 2 / 128 / 129
+    ([1, 250, 127, 384, 64], 6, 2, 64),             # head_dim 64, group 3
+    ([1100], 1, 1, 128),                            # one document, 9 tiles
+    ([700, 33, 1290], 7, 1, 128),                   # group 7 (one sequence-parallel rank of 56 / 8)
+    ([256, 255, 257], 2, 2, 128),
+])
+def test_small_cases_full_compare(ops, lens, Hq, Hkv, d):
+    _check_full(ops, lens, Hq, Hkv, d, seed=sum(lens) % 97)
+
+
+def test_bf16_gradient_output(ops):
+    _check_full(ops, [400, 77, 900], 4, 4, 128, seed=3, grad_dtype=torch.bfloat16)
+
+
+def test_custom_scale_and_scaled_q(ops):
+    """softmax_scale other than 1/sqrt(d). The logits keep unit spread
+    (q drawn as N(0, 1) / sqrt(128) when the scale is 1): with N(0, 1) q and
+    k and scale 1 they would spread as N(0, 128), a softmax so sharp that the
+    bf16 rounding of dS alone exceeds the gradient bar for any bf16 MMA."""
+    _check_full(ops, [333, 555], 4, 2, 128, seed=4, scale=1.0, q_scale=1.0 / np.sqrt(128.0))
+    _check_full(ops, [333, 555], 4, 2, 128, seed=5, q_scale=1.0 / np.sqrt(128.0))
+    _check_full(ops, [100, 901], 2, 1, 64, seed=6, scale=0.2)
+
+
+def test_length_one_documents(ops):
+    """P = 1 for every row: O equals V bit for bit; dQ, dK vanish; dV is the
+    group sum of dO."""
+    out, lse, dq, dk, dv, (qn, kn, vn, don, cu) = _check_full(ops, [1] * 200, 4, 2, 128, seed=6)
+    o = out.cpu()
+    vv = torch.from_numpy(vn.view(np.int16)).view(torch.bfloat16)
+    for h in range(4):
+        assert torch.equal(o[:, h, :], vv[:, h // 2, :])
+    assert float(dq.abs().max()) < 1e-4 and float(dk.abs().max()) < 1e-4
+
+
+def test_packed_row_from_pack_kernel(ops):
+    """The pipeline: pack_tokens' cu_seqlens (documents split across rows and a
+    padding tail) feed the attention calls directly."""
+    rng = np.random.default_rng(12)
+    lens = rng.integers(20, 700, size=17).astype(np.int32)
+    toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+    mb, sl = 2, 1024
+    po = ops.pack_tokens(torch.tensor(toks, device="cuda"), torch.tensor(lens, device="cuda"), mb, sl, True)
+    ns = int(po["num_segs"].item())
+    cu_gpu = po["cu_seqlens"][:ns + 1].cpu().numpy()
+    ref = P.pack_flat([toks[a:b].tolist() for a, b in zip(np.r_[0, np.cumsum(lens)[:-1]], np.cumsum(lens))],
+                      mb, sl, True)
+    np.testing.assert_array_equal(cu_gpu, ref["cu_seqlens"])
+    lens_seg = np.diff(cu_gpu)
+    _check_full(ops, lens_seg.tolist(), 4, 2, 128, seed=7)
+
+
+def test_mid_size_full_compare(ops):
+    rng = np.random.default_rng(21)
+    lens = rng.integers(1, 1500, size=9).tolist() + [3000]
+    _check_full(ops, lens, 4, 2, 128, seed=8)
+
+
+def test_bad_seqlens_set_status(ops):
+    q, k, v, do = _inputs(512, 2, 2, 128, 1)
+    for cu in ([0, 300, 200, 512], [0, 300, 511], [1, 300, 512], [0, 300, 300, 512]):
+        cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+        ws = ops.workspace(ops.attn_workspace_size(512, len(cu) - 1, 2, 2, 128, True))
+        ops.varlen_attn_fwd(q, k, v, cu_t, len(cu) - 1, ws=ws)
+        assert ops.read_status(ws) == -4
+        out = torch.zeros_like(q)
+        lse = torch.zeros(2, 512, device="cuda")
+        ops.varlen_attn_bwd(q, k, v, out, do, lse, cu_t, len(cu) - 1, ws=ws)
+        assert ops.read_status(ws) == -4
+    cu_t = torch.tensor([0, 200, 512], dtype=torch.int32, device="cuda")   # the context is still good
+    ws = ops.workspace(ops.attn_workspace_size(512, 2, 2, 2, 128, False))
+    ops.varlen_attn_fwd(q, k, v, cu_t, 2, ws=ws)
+    assert ops.read_status(ws) == 0
+
+
+# ----------------------------------------------------------------------------- full size
+
+def _workload_inputs(name):
+    from sample_packing_document_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    lens, toks = W.documents(w)
+    flat = OA.pack(toks, lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
+    cu = flat["cu_seqlens"]
+    T = int(cu[-1])
+    q, k, v, do = _inputs(T, w.Hq, w.Hkv, w.head_dim, w.seed, q_scale=w.q_scale)
+    return w, cu, q, k, v, do
+
+
+@pytest.mark.parametrize("name", ["tiny", "c2", "c3", "c4", "c5"])
+def test_workload_full_size_sampled(ops, name):
+    w, cu, q, k, v, do = _workload_inputs(name)
+    T, Hq = q.shape[0], q.shape[1]
+    out, lse, dq, dk, dv = _run(ops, q, k, v, do, cu)
+    for t in (out, lse, dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    qn, kn, vn, don = _u16(q), _u16(k), _u16(v), _u16(do)
+    rng = np.random.default_rng(77)
+    lens = np.diff(cu)
+    longest = int(np.argmax(lens))
+    rows = list(rng.integers(0, T, size=96))
+    rows += [int(cu[longest]), int(cu[longest + 1]) - 1, int(cu[longest + 1]) - 129, int(cu[1]) - 1]
+    rows = [r for r in rows if 0 <= r < T]
+    items = np.array([(int(rng.integers(0, Hq)) * T + r) for r in rows], np.int64)
+    o_ref, lse_ref = OA.attn_fwd(qn, kn, vn, cu, items=items)
+    o_gpu = out.float().cpu().numpy().reshape(T, Hq, -1)
+    lse_gpu = lse.cpu().numpy()
+    for n, it in enumerate(items):
+        h, i = divmod(int(it), T)
+        assert _maxerr(o_gpu[i, h], o_ref[n]) <= TOL_O
+        assert abs(float(lse_gpu[h, i]) - lse_ref[n]) <= TOL_LSE
+    dq_items = items[:48]
+    dq_ref = OA.attn_dq_rows(qn, kn, vn, don, cu, dq_items)
+    dq_gpu = dq.cpu().numpy()
+    for n, it in enumerate(dq_items):
+        h, i = divmod(int(it), T)
+        assert _maxerr(dq_gpu[i, h], dq_ref[n]) <= TOL_G
+    # dK / dV: whole segments, the shortest ones and one of up to 2048 tokens
+    order = np.argsort(lens, kind="stable")
+    segs = [int(s) for s in order[:3]]
+    mid = [int(s) for s in order if lens[s] <= 2048]
+    if mid and mid[-1] not in segs:
+        segs.append(mid[-1])
+    gq, gk, gv, srows = OA.attn_bwd(qn, kn, vn, don, cu, segs=segs)
+    assert _maxerr(dk.cpu().numpy()[srows], gk) <= TOL_G
+    assert _maxerr(dv.cpu().numpy()[srows], gv) <= TOL_G
+    assert _maxerr(dq.cpu().numpy()[srows], gq) <= TOL_G

@@ -1,0 +1,134 @@
+"""GPU parity of spd_pack_tokens: bit-exact against the oracle.
+
+Cases: the worked examples of the InternEvo page "Data loading and flow";
+thousands of random tiny cases (carry-over across rows, padding, length-1
+documents, documents longer than a row, both modes); the five workloads at
+full size; unaligned outputs (scalar store path); bad document lengths
+(status word, no fault).
+"""
+import json
+import os
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as OA
+from oracle import pack as P
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pack_examples.json")))
+
+
+@pytest.fixture(scope="module")
+def ops():
+    from sample_packing_document_gb300 import build, ops as _ops
+    build.build()
+    _ops.load()
+    return _ops
+
+
+def _gpu_pack(ops, toks, lens, mb, sl, packed):
+    t = torch.tensor(np.asarray(toks, np.int32), device="cuda")
+    l = torch.tensor(np.asarray(lens, np.int32), device="cuda")
+    out = ops.pack_tokens(t, l, mb, sl, packed)
+    st = ops.read_status(out["ws"])
+    ns = int(out["num_segs"].item())
+    rows = out["rows"]
+    return st, {
+        "input_ids": out["input_ids"].cpu().numpy(), "labels": out["labels"].cpu().numpy(),
+        "indexes": out["indexes"].cpu().numpy(), "cu_seqlens": out["cu_seqlens"][:ns + 1].cpu().numpy(),
+        "row_seg_ptr": out["row_seg_ptr"].cpu().numpy(), "max_seqlen": out["max_seqlen"][:rows].cpu().numpy(),
+        "num_segs": ns, "rows": rows}
+
+
+def _assert_same(g, ref):
+    assert g["rows"] == ref["rows"]
+    assert g["num_segs"] == ref["num_segs"]
+    for key in ("input_ids", "labels", "indexes", "cu_seqlens", "row_seg_ptr", "max_seqlen"):
+        np.testing.assert_array_equal(np.asarray(g[key]), np.asarray(ref[key], dtype=np.int32), err_msg=key)
+
+
+def test_worked_examples(ops):
+    for key in ("build_pack", "build_unpack"):
+        gd = GOLDEN[key]
+        docs = gd["docs"]
+        st, g = _gpu_pack(ops, [t for d in docs for t in d], [len(d) for d in docs], gd["micro_bsz"],
+                          gd["seq_len"], gd["use_packed_dataset"])
+        assert st == 0
+        rows = len(gd["input_ids"])
+        assert g["input_ids"].reshape(rows, -1).tolist() == gd["input_ids"]
+        assert g["labels"].reshape(rows, -1).tolist() == gd["labels"]
+        _assert_same(g, P.pack_flat(docs, gd["micro_bsz"], gd["seq_len"], gd["use_packed_dataset"]))
+    st, g = _gpu_pack(ops, [t for d in GOLDEN["build_pack"]["docs"] for t in d],
+                      [len(d) for d in GOLDEN["build_pack"]["docs"]], 2, 8, True)
+    assert g["indexes"].reshape(2, -1).tolist() == GOLDEN["batch_fields"]["indexes"]
+    assert g["cu_seqlens"].tolist() == [0, 4, 11, 16, 19, 24, 32]
+    assert g["max_seqlen"][0] == GOLDEN["batch_fields"]["max_seqlen_row0"]
+
+
+@pytest.mark.parametrize("packed", [True, False])
+def test_random_tiny_cases(ops, packed):
+    rng = random.Random(4242 + packed)
+    for _ in range(1500):
+        mb, sl = rng.randint(1, 4), rng.randint(1, 16)
+        plen = mb * sl
+        n = rng.randint(1, 10)
+        docs = [[rng.randint(1, 49999) for _ in range(rng.randint(1, 3 * plen))] for _ in range(n)]
+        st, g = _gpu_pack(ops, [t for d in docs for t in d], [len(d) for d in docs], mb, sl, packed)
+        assert st == 0
+        _assert_same(g, P.pack_flat(docs, mb, sl, packed))
+
+
+@pytest.mark.parametrize("packed", [True, False])
+def test_many_docs_multi_pass_scan(ops, packed):
+    """More documents than one pass of the scan covers (4096 per pass)."""
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 9, size=20000).astype(np.int32)
+    toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+    for mb, sl in ((3, 7), (1, 64), (8, 1)):
+        st, g = _gpu_pack(ops, toks, lens, mb, sl, packed)
+        assert st == 0
+        _assert_same(g, OA.pack(toks, lens, mb, sl, packed))
+
+
+@pytest.mark.parametrize("name", ["tiny", "c2", "c3", "c3_unpack", "c4", "c5"])
+def test_workloads_full_size(ops, name):
+    from sample_packing_document_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    lens, toks = W.documents(w)
+    st, g = _gpu_pack(ops, toks, lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
+    assert st == 0
+    _assert_same(g, OA.pack(toks, lens, w.micro_bsz, w.seq_len, w.use_packed_dataset))
+
+
+def test_unaligned_outputs_take_scalar_path(ops):
+    rng = np.random.default_rng(9)
+    lens = rng.integers(1, 40, size=300).astype(np.int32)
+    toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+    mb, sl = 2, 33
+    ref = OA.pack(toks, lens, mb, sl, True)
+    n = ref["rows"] * mb * sl
+    base = torch.zeros(3 * n + 8, dtype=torch.int32, device="cuda")
+    out = ops.alloc_pack_outputs(len(lens), len(toks), mb, sl, True)
+    out["input_ids"], out["labels"], out["indexes"] = base[1:1 + n], base[2 + n:2 + 2 * n], base[3 + 2 * n:3 + 3 * n]
+    tb = torch.zeros(len(toks) + 1, dtype=torch.int32, device="cuda")
+    tb[1:] = torch.tensor(toks, device="cuda")
+    t = tb[1:]                                           # unaligned tokens too
+    ops.pack_tokens(t, torch.tensor(lens, device="cuda"), mb, sl, True, out=out)
+    assert ops.read_status(out["ws"]) == 0
+    np.testing.assert_array_equal(out["input_ids"].cpu().numpy(), ref["input_ids"])
+    np.testing.assert_array_equal(out["labels"].cpu().numpy(), ref["labels"])
+    np.testing.assert_array_equal(out["indexes"].cpu().numpy(), ref["indexes"])
+
+
+def test_bad_doc_lengths_set_status(ops):
+    toks = torch.arange(1, 11, dtype=torch.int32, device="cuda")
+    st, _ = _gpu_pack(ops, toks.cpu().numpy(), [4, 0, 6], 2, 4, True)
+    assert st == -7
+    st, _ = _gpu_pack(ops, toks.cpu().numpy(), [4, 5, 2], 2, 4, True)   # sums to 11, not 10
+    assert st == -7
+    st, g = _gpu_pack(ops, toks.cpu().numpy(), [4, 6], 2, 4, True)      # and the next call is clean
+    assert st == 0 and g["num_segs"] == 4 and g["cu_seqlens"].tolist() == [0, 4, 8, 10, 16]
