@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Throughput of the packed-training hot path on GB300.
+
+One step = the whole path over one batch of synthetic input already resident
+in HBM: spd_pack_tokens (documents -> packed rows, cu_seqlens), then
+spd_varlen_attn_fwd and spd_varlen_attn_bwd over the packed rows.
+
+metric: unmasked attention FLOPs (fwd + bwd) per second. Only the entries of
+the per-document causal mask count: pairs = sum over segments L (L + 1) / 2,
+fwd = 4 d Hq pairs, bwd = 2.5 x fwd (five GEMMs including the S recompute);
+the strict count (bwd = 2 x fwd) is printed beside it.
+
+Default workload: 4 packed rows of 8192 tokens (micro_num 4, micro_bsz 2,
+SEQ_LEN 4096), lognormal document lengths (median 600), 32 q / 32 kv heads,
+head_dim 128, bf16. Inputs (256 MB per tensor) exceed the 129 MB L2, so no
+flush runs between steps.
+
+  python bench.py [--gpus N --steps K --warmup W] [--workload c2|c3|c4|c5|tiny]
+  python bench.py --impl reference ...     # the CPU oracle as the reference arm
+
+Several GPUs (torchrun): each rank runs an independent replica of the same
+step (the path has no exchange step); rank 0 prints the aggregate.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed varlen causal attn fwd+bwd TFLOP/s (unmasked FLOPs), % bf16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_docs(name):
+    from sample_packing_document_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    lens, toks = W.documents(w)
+    return w, lens, toks
+
+
+def segment_lengths(lens, w):
+    """Segment lengths of the packed rows (host arithmetic for the FLOP count
+    only; the kernels compute cu_seqlens themselves every step)."""
+    plen = w.micro_bsz * w.seq_len
+    if w.use_packed_dataset:
+        starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+        total = int(lens.sum())
+        rows = -(-total // plen)
+        b = set(starts.tolist()) | set(range(0, rows * plen + 1, plen)) | {total}
+        b = np.array(sorted(b))
+        return np.diff(b)
+    segs = []
+    for r in range(0, len(lens), w.micro_bsz):
+        kept = np.minimum(lens[r:r + w.micro_bsz], w.seq_len)
+        segs += kept.tolist()
+        if kept.sum() < plen:
+            segs.append(plen - int(kept.sum()))
+    return np.array(segs)
+
+
+def flops(seg_lens, Hq, d):
+    pairs = float(np.sum(seg_lens.astype(np.float64) * (seg_lens + 1) / 2))
+    fwd = 4.0 * d * Hq * pairs
+    return {"pairs": pairs, "fwd": fwd, "bwd": 2.5 * fwd, "total": 3.5 * fwd, "strict_total": 3.0 * fwd}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "spd_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    mhz.append(float(f[1]))
+                    mx = float(f[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        finally:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_max(value, ws):
+    """Max of a host float over ranks (gloo on host tensors; timing only)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(w, seg_lens, cu, budget_pairs):
+    """Whole segments, in a fixed shuffled order, until the unmasked pair count
+    reaches budget_pairs (all heads of each segment are computed)."""
+    rng = np.random.default_rng(2024)
+    order = rng.permutation(len(seg_lens))
+    chosen, pairs = [], 0.0
+    for s in order:
+        L = float(seg_lens[s])
+        if chosen and pairs + L * (L + 1) / 2 > budget_pairs:
+            continue
+        chosen.append(int(s))
+        pairs += L * (L + 1) / 2
+        if pairs >= budget_pairs:
+            break
+    return sorted(chosen), pairs
+
+
+def run_oracle_once(q16, k16, v16, do16, cu, segs, scale, nthreads):
+    """fwd + bwd of the oracle over the chosen segments; returns seconds."""
+    from oracle import attention as OA
+    T = q16.shape[0]
+    Hq = q16.shape[1]
+    items = np.concatenate([np.arange(cu[s], cu[s + 1]) for s in segs])
+    items = (np.arange(Hq)[:, None] * T + items[None, :]).reshape(-1)
+    t0 = time.perf_counter()
+    OA.attn_fwd(q16, k16, v16, cu, scale=scale, items=items, nthreads=nthreads)
+    OA.attn_bwd(q16, k16, v16, do16, cu, segs=segs, scale=scale, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_inputs(w, T):
+    import torch
+    from sample_packing_document_gb300 import workloads as W
+    q, k, v, do = W.qkv(T, w.Hq, w.Hkv, w.head_dim, w.seed, device="cpu", q_scale=w.q_scale)
+    u = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    return u(q), u(k), u(v), u(do)
+
+
+def oracle_inputs_for(w, seg_lens):
+    cu = np.concatenate([[0], np.cumsum(seg_lens)]).astype(np.int32)
+    return cu
+
+
+def cpu_baseline(w, seg_lens, target_s=12.0):
+    """The oracle as it stands, on this host's cores, on a bounded sample."""
+    from oracle import build as OB
+    OB.build()
+    cores = len(os.sched_getaffinity(0))
+    cu = oracle_inputs_for(w, seg_lens)
+    q16, k16, v16, do16 = cpu_inputs(w, int(cu[-1]))
+    scale = 1.0 / np.sqrt(w.head_dim)
+    # calibrate on a small sample, then size the sample to ~target_s
+    segs, pairs = oracle_sample(w, seg_lens, cu, 2.0e5)
+    t = run_oracle_once(q16, k16, v16, do16, cu, segs, scale, cores)
+    rate = pairs / max(t, 1e-3)
+    segs, pairs = oracle_sample(w, seg_lens, cu, rate * target_s)
+    t = run_oracle_once(q16, k16, v16, do16, cu, segs, scale, cores)
+    f = 14.0 * w.head_dim * w.Hq * pairs
+    return {"value": f / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "fp64 oracle fwd+bwd over %d whole segments (%.3g of %.3g unmasked pairs, all %d heads), %.1f s"
+                      % (len(segs), pairs, float(np.sum(seg_lens * (seg_lens + 1.0) / 2)), w.Hq, t)}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed as the reference arm."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w, lens, toks = workload_docs(args.workload)
+    seg_lens = segment_lengths(lens, w)
+    from oracle import build as OB
+    OB.build()
+    cores = len(os.sched_getaffinity(0))
+    cu = oracle_inputs_for(w, seg_lens)
+    q16, k16, v16, do16 = cpu_inputs(w, int(cu[-1]))
+    scale = 1.0 / np.sqrt(w.head_dim)
+    # each step: a bounded sample sized so the whole run stays within minutes
+    n_total = args.steps + args.warmup
+    per_step = max(0.5, min(6.0, 150.0 / max(n_total, 1)))
+    segs, pairs = oracle_sample(w, seg_lens, cu, 2.0e5)
+    t = run_oracle_once(q16, k16, v16, do16, cu, segs, scale, cores)
+    segs, pairs = oracle_sample(w, seg_lens, cu, pairs / max(t, 1e-3) * per_step)
+    for _ in range(args.warmup):
+        run_oracle_once(q16, k16, v16, do16, cu, segs, scale, cores)
+    times = [run_oracle_once(q16, k16, v16, do16, cu, segs, scale, cores) for _ in range(args.steps)]
+    total = sum(times)
+    f = 14.0 * w.head_dim * w.Hq * pairs
+    value = f * args.steps / total / 1e12
+    sample = "fp64 oracle fwd+bwd over %d whole segments per step (%.3g unmasked pairs, all %d heads)" % (
+        len(segs), pairs, w.Hq)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, seg_lens),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w, seg_lens):
+    return {"workload": "%s: %d tokens in %d packed row(s) (micro_bsz %d, SEQ_LEN %d, use_packed_dataset=%s), "
+                        "%d segments, Hq %d / Hkv %d, head_dim %d" % (
+                            w.name, int(seg_lens.sum()), -(-int(seg_lens.sum()) // (w.micro_bsz * w.seq_len)),
+                            w.micro_bsz, w.seq_len, w.use_packed_dataset, len(seg_lens), w.Hq, w.Hkv,
+                            w.head_dim),
+            "tokens": int(seg_lens.sum()), "segments": int(len(seg_lens)), "max_segment": int(seg_lens.max()),
+            "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.head_dim,
+            "l2": "inputs larger than L2 (no flush)" if int(seg_lens.sum()) * w.Hq * w.head_dim * 2 > 129e6
+            else "L2 flushed between steps"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from sample_packing_document_gb300 import ops
+    from sample_packing_document_gb300 import workloads as W
+
+    w, lens, toks = workload_docs(args.workload)
+    seg_lens = segment_lengths(lens, w)
+    fl = flops(seg_lens, w.Hq, w.head_dim)
+    T = int(seg_lens.sum())
+    d, Hq, Hkv = w.head_dim, w.Hq, w.Hkv
+
+    # inputs resident in HBM
+    toks_d = torch.tensor(toks, device=dev)
+    lens_d = torch.tensor(lens, device=dev)
+    q, k, v, do = W.qkv(T, Hq, Hkv, d, w.seed, device=dev, q_scale=w.q_scale)
+    pk = ops.alloc_pack_outputs(len(lens), len(toks), w.micro_bsz, w.seq_len, w.use_packed_dataset, dev)
+    ops.pack_tokens(toks_d, lens_d, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk)
+    ns = int(pk["num_segs"].item())    # same documents every step: read back once
+    assert ns == len(seg_lens), (ns, len(seg_lens))
+    cu = pk["cu_seqlens"]
+    out = torch.empty_like(q)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=dev)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws_f = ops.workspace(ops.attn_workspace_size(T, ns, Hq, Hkv, d, False), dev)
+    ws_b = ops.workspace(ops.attn_workspace_size(T, ns, Hq, Hkv, d, True), dev)
+
+    def step():
+        ops.pack_tokens(toks_d, lens_d, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk)
+        ops.varlen_attn_fwd(q, k, v, cu, ns, out=out, lse=lse, ws=ws_f)
+        ops.varlen_attn_bwd(q, k, v, out, do, lse, cu, ns, dq=dq, dk=dk, dv=dv, ws=ws_b)
+
+    launches_per_step = 2 + 2 + 4   # pack: scan + stream; fwd: schedule + main; bwd: schedule + pre + main + dq
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    for wsp in (pk["ws"], ws_f, ws_b):
+        st = ops.read_status(wsp)
+        if st != 0:
+            raise RuntimeError("device status %d (%s)" % (st, ops.status_string(st)))
+
+    # timed region: K steps, barrier + synchronize on both sides, per-kernel events
+    stream = torch.cuda.current_stream()
+    ev = {kname: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)] for kname in ("fwd", "bwd")}
+    for pair in ev["fwd"] + ev["bwd"]:
+        for e in pair:
+            e.record(stream)    # creates the CUDA event; the library re-records it around its kernel
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        dist_barrier(ws_n)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            ops.pack_tokens(toks_d, lens_d, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk)
+            ops.set_profile_events(*ev["fwd"][i], ops.PROFILE_ATTN_FWD)
+            ops.varlen_attn_fwd(q, k, v, cu, ns, out=out, lse=lse, ws=ws_f)
+            ops.set_profile_events(*ev["bwd"][i], ops.PROFILE_ATTN_BWD)
+            ops.varlen_attn_bwd(q, k, v, out, do, lse, cu, ns, dq=dq, dk=dk, dv=dv, ws=ws_b)
+            ops.set_profile_events(None, None, ops.PROFILE_NONE)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(ws_n)
+    clocks = clk.summary()
+    ms_local = t_start.elapsed_time(t_end) / args.steps
+    ms = dist_max(ms_local, ws_n)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["fwd"])
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["bwd"])
+    value = ws_n * fl["total"] / (ms * 1e-3) / 1e12
+
+    pk_, how = peaks()
+    peak = pk_.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    bwd_tf = fl["bwd"] / (bwd_ms * 1e-3) / 1e12
+    roofline = {"kernel": "attn_bwd_kernel (main backward kernel, %d%% of step time)" % round(100 * bwd_ms / ms),
+                "bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
+                "frac": bwd_tf / peak, "traffic": None,
+                "peak_source": "%s bf16_tflops_sustained (kernel timed inside the step loop)" % how,
+                "flops_per_launch": fl["bwd"], "ms_per_launch": bwd_ms}
+    fwd_tf = fl["fwd"] / (fwd_ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev)
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, seg_lens)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded documents and N(0,1) q/k/v/dO)",
+                "config": workload_config(w, seg_lens),
+                "pct_bf16_peak": {"sustained": 100 * value / ws_n / peak,
+                                  "burst": 100 * value / ws_n / pk_.get("bf16_tflops", 1900.0)},
+                "flops_per_step": fl["total"], "strict_flops_value": ws_n * fl["strict_total"] / (ms * 1e-3) / 1e12,
+                "kernels_ms": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms},
+                "kernels_tflops": {"attn_fwd": fwd_tf, "attn_bwd": bwd_tf},
+                "roofline": roofline, "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "cpu_baseline": cpu}
+        print(json.dumps(line))
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
+    """Same metric through the public API with host buffers: every step copies
+    the documents and q / k / v / dO from pinned host memory, packs, runs
+    forward and backward, and reads dQ / dK / dV back to pinned host memory."""
+    import torch
+    h = lambda t: t.cpu().pin_memory()
+    toks_h, lens_h = torch.tensor(toks).pin_memory(), torch.tensor(lens).pin_memory()
+    q_h, k_h, v_h, do_h = h(q), h(k), h(v), h(do)
+    dq_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    dk_h = torch.empty(k.shape, dtype=k.dtype).pin_memory()
+    dv_h = torch.empty(v.shape, dtype=v.dtype).pin_memory()
+    d_toks, d_lens = torch.empty_like(toks_h, device=dev), torch.empty_like(lens_h, device=dev)
+    d_q, d_k, d_v, d_do = (torch.empty_like(x, device=dev) for x in (q_h, k_h, v_h, do_h))
+    seg_lens = segment_lengths(lens, w)
+    fl = flops(seg_lens, w.Hq, w.head_dim)
+
+    def one():
+        for dst, src in ((d_toks, toks_h), (d_lens, lens_h), (d_q, q_h), (d_k, k_h), (d_v, v_h), (d_do, do_h)):
+            dst.copy_(src, non_blocking=True)
+        pk = ops.pack_tokens(d_toks, d_lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
+        ns = int(pk["num_segs"].item())
+        o, lse = ops.varlen_attn_fwd(d_q, d_k, d_v, pk["cu_seqlens"], ns)
+        gq, gk, gv = ops.varlen_attn_bwd(d_q, d_k, d_v, o, d_do, lse, pk["cu_seqlens"], ns)
+        dq_h.copy_(gq, non_blocking=True)
+        dk_h.copy_(gk, non_blocking=True)
+        dv_h.copy_(gv, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    n = max(2, min(args.steps, 5))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    h2d = sum(x.numel() * x.element_size() for x in (toks_h, lens_h, q_h, k_h, v_h, do_h))
+    d2h = 4 + sum(x.numel() * x.element_size() for x in (dq_h, dk_h, dv_h))
+    return {"value": fl["total"] / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

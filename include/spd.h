@@ -67,6 +67,24 @@ const char *spd_status_string(int status);
 int spd_version(void);
 
 /*
+ * Measurement hook. For the calling host thread, make the launcher of one
+ * kernel record `begin_event` / `end_event` (cudaEvent_t handles created by
+ * the caller) on the launch stream immediately before and after that kernel,
+ * so its duration can be read with cudaEventElapsedTime. kernel:
+ * SPD_PROFILE_NONE (off), SPD_PROFILE_PACK_STREAM (the token-stream kernel of
+ * spd_pack_tokens), SPD_PROFILE_ATTN_FWD / SPD_PROFILE_ATTN_BWD (the main
+ * attention kernel of each call, without the scheduling and pre/post-pass
+ * kernels). Null events turn it off. Returns SPD_OK or SPD_ERR_INVALID_ARG.
+ */
+enum {
+    SPD_PROFILE_NONE = 0,
+    SPD_PROFILE_PACK_STREAM = 1,
+    SPD_PROFILE_ATTN_FWD = 2,
+    SPD_PROFILE_ATTN_BWD = 3
+};
+int spd_set_profile_events(void *begin_event, void *end_event, int kernel);
+
+/*
  * Synchronise `stream` and return the device status word of the last call
  * that used workspace `ws` (SPD_OK or a negative SPD_ERR_* code) in
  * *device_status (host). Returns SPD_OK or SPD_ERR_CUDA.

@@ -110,6 +110,13 @@ int clear_status(void *ws, cudaStream_t stream)
 }
 
 }  // namespace
+
+ProfileHook &profile_hook()
+{
+    static thread_local ProfileHook hook;
+    return hook;
+}
+
 }  // namespace spd
 
 using namespace spd;
@@ -132,6 +139,16 @@ const char *spd_status_string(int s)
 }
 
 int spd_version(void) { return 100; }
+
+int spd_set_profile_events(void *begin_event, void *end_event, int kernel)
+{
+    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_ATTN_BWD) return SPD_ERR_INVALID_ARG;
+    ProfileHook &h = profile_hook();
+    h.begin = static_cast<cudaEvent_t>(begin_event);
+    h.end = static_cast<cudaEvent_t>(end_event);
+    h.which = (begin_event && end_event) ? kernel : kProfNone;
+    return SPD_OK;
+}
 
 int spd_read_status(const void *ws, spd_stream_t stream, int *device_status)
 {

@@ -499,7 +499,9 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t 
     const int64_t grid = grid_tiles * a.Hkv;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (grid > 0) {
+        prof_begin(kProfAttnBwd, stream);
         attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+        prof_end(kProfAttnBwd, stream);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -305,7 +305,9 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, int64_t grid_tiles, cudaStream_t 
     const int64_t grid = grid_tiles * a.Hq;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    prof_begin(kProfAttnFwd, stream);
     attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+    prof_end(kProfAttnFwd, stream);
     return cudaGetLastError();
 }
 

@@ -9,6 +9,27 @@
 
 namespace spd {
 
+// Measurement hook (spd_set_profile_events): when `which` names a kernel,
+// its launcher records `begin` / `end` on the launch stream around that one
+// kernel. Per host thread.
+enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3 };
+struct ProfileHook {
+    cudaEvent_t begin = nullptr, end = nullptr;
+    int which = kProfNone;
+};
+ProfileHook &profile_hook();
+
+inline void prof_begin(int which, cudaStream_t s)
+{
+    ProfileHook &h = profile_hook();
+    if (h.which == which && h.begin) cudaEventRecord(h.begin, s);
+}
+inline void prof_end(int which, cudaStream_t s)
+{
+    ProfileHook &h = profile_hook();
+    if (h.which == which && h.end) cudaEventRecord(h.end, s);
+}
+
 // Workspace header: [0] status word, [1] tile count; the rest per operation.
 constexpr size_t kWsHeader = 256;
 

@@ -359,8 +359,11 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (a.packed) return cudaLaunchKernelEx(&cfg, pack_stream_kernel<true>, a);
-    return cudaLaunchKernelEx(&cfg, pack_stream_kernel<false>, a);
+    prof_begin(kProfPackStream, stream);
+    e = a.packed ? cudaLaunchKernelEx(&cfg, pack_stream_kernel<true>, a)
+                 : cudaLaunchKernelEx(&cfg, pack_stream_kernel<false>, a);
+    prof_end(kProfPackStream, stream);
+    return e;
 }
 
 }  // namespace spd

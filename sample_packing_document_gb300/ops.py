@@ -25,6 +25,7 @@ SIGNATURES = {
     "spd_status_string": (ctypes.c_char_p, [_INT]),
     "spd_version": (_INT, []),
     "spd_read_status": (_INT, [_P, _P, ctypes.POINTER(_INT)]),
+    "spd_set_profile_events": (_INT, [_P, _P, _INT]),
     "spd_pack_rows": (_INT, [_I64, _I64, _INT, _INT, _INT, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "spd_pack_workspace_size": (_SZ, [_I64]),
     "spd_pack_tokens": (_INT, [_P, _P, _I64, _I64, _INT, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -93,6 +94,17 @@ def read_status(ws, stream=None):
     v = _INT(0)
     _check("spd_read_status", load().spd_read_status(_ptr(ws), _stream(stream), ctypes.byref(v)))
     return v.value
+
+
+PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD = 0, 1, 2, 3
+
+
+def set_profile_events(begin, end, kernel):
+    """Record torch.cuda.Event pair (begin, end) around one library kernel of
+    the following calls on this thread (see spd_set_profile_events)."""
+    b = ctypes.c_void_p(begin.cuda_event) if begin is not None else None
+    e = ctypes.c_void_p(end.cuda_event) if end is not None else None
+    _check("spd_set_profile_events", load().spd_set_profile_events(b, e, int(kernel)))
 
 
 # ----------------------------------------------------------------------------- packing

@@ -58,13 +58,16 @@ WORKLOADS = {
                           q_scale=1.0 / np.sqrt(128.0)),
     "c4": Workload("c4", 3, 1, 131072, True, 131072, 7, 1, 128),
     "c5": Workload("c5", 4, 1, 1048576, True, 1048576, 4, 4, 128),
+    # c2's documents with 16 / 16 heads: a smaller device footprint for
+    # hardware-counter captures (inputs still larger than L2).
+    "c2p": Workload("c2p", 1, 2, 4096, True, 32768, 16, 16, 128),
 }
 
 
 def _draw_length(name, rng):
     if name == "tiny":
         return int(rng.integers(1, 65))
-    if name == "c2":
+    if name in ("c2", "c2p"):
         return int(np.clip(np.rint(np.exp(rng.normal(np.log(600.0), 1.0))), 16, 8192))
     if name.startswith("c3"):
         if rng.random() < 0.7:
