@@ -57,7 +57,8 @@ enum {
     SPD_ERR_BAD_SEQLENS = -4,    /* device: cu_seqlens not 0 = c0 < c1 < ... = total */
     SPD_ERR_DEVICE_TIMEOUT = -5, /* device: a bounded wait ran out */
     SPD_ERR_WORKSPACE = -6,      /* host: workspace too small or misaligned */
-    SPD_ERR_BAD_DOCS = -7        /* device: a document length <= 0 or sum != num_tokens */
+    SPD_ERR_BAD_DOCS = -7,       /* device: a document length <= 0 or sum != num_tokens */
+    SPD_ERR_TOO_LARGE = -8       /* host: problem exceeds the fixed scratch of a no-allocation entry point */
 };
 
 /* Text for a status code (static storage). */
@@ -211,6 +212,40 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         int32_t max_seqlen, int Hq, int Hkv, int head_dim, float softmax_scale,
                         int grad_dtype, void *dq, void *dk, void *dv, void *ws,
                         size_t ws_bytes, spd_stream_t stream);
+
+/*
+ * Forward attention without any workspace, for callers that cannot allocate
+ * device memory: code that runs inside a host framework which owns all device
+ * memory and hands out only the tensors of the operation, or a latency-critical
+ * path that must not call cudaMalloc / cudaFree (which can synchronise the
+ * whole device) and keeps no buffers of its own.
+ *
+ * The pages this library follows have no counterpart to this entry point; it
+ * computes exactly what spd_varlen_attn_fwd computes, with the same argument
+ * meaning, layouts and host checks, minus ws / ws_bytes, and allocates nothing.
+ * Its scratch (status word and tile work list) is one fixed array of
+ * SPD_NOALLOC_SCRATCH_BYTES in the library's device image: every GPU that loads
+ * the library holds it until the process exits. Problems whose scratch would
+ * not fit (spd_attn_workspace_size(..., bwd = 0) > SPD_NOALLOC_SCRATCH_BYTES;
+ * about 250k tiles, e.g. 16M tokens in a few thousand documents) return
+ * SPD_ERR_TOO_LARGE before anything is launched.
+ *
+ * The first call on each device looks up the array's device address with that
+ * device current (a runtime symbol query, no allocation); make that first call
+ * before any stream capture. All calls share the one array and the array keeps
+ * the last call's contents (each call rewrites what it reads), so calls that
+ * overlap on the GPU -- on different streams, or from different threads --
+ * race: serialise them.
+ *
+ * device_status (device pointer to one int32, may be NULL) receives the call's
+ * device status word (SPD_OK or SPD_ERR_BAD_SEQLENS / SPD_ERR_DEVICE_TIMEOUT),
+ * written on `stream` after the kernels.
+ */
+#define SPD_NOALLOC_SCRATCH_BYTES (4u << 20)
+int spd_varlen_attn_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
+                                int32_t max_seqlen, int Hq, int Hkv, int head_dim, float softmax_scale,
+                                uint16_t *out, float *lse, int32_t *device_status, spd_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -134,6 +134,7 @@ const char *spd_status_string(int s)
     case SPD_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out";
     case SPD_ERR_WORKSPACE: return "workspace too small or misaligned";
     case SPD_ERR_BAD_DOCS: return "a document length <= 0 or lengths do not sum to num_tokens";
+    case SPD_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
     }
 }

@@ -33,6 +33,8 @@ SIGNATURES = {
     "spd_varlen_attn_fwd": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _P, _P, _P, _SZ, _P]),
     "spd_varlen_attn_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _INT,
                                    _P, _P, _P, _P, _SZ, _P]),
+    "spd_varlen_attn_fwd_noalloc": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _P, _P, _P,
+                                           _P]),
 }
 
 
@@ -213,3 +215,17 @@ def varlen_attn_bwd(q, k, v, out, dout, lse, cu_seqlens, num_segs, max_seqlen=0,
 
 def default_scale(head_dim):
     return 1.0 / math.sqrt(head_dim)
+
+
+def varlen_attn_fwd_noalloc(q, k, v, cu_seqlens, num_segs, out, lse, device_status=None, max_seqlen=0,
+                            softmax_scale=None, stream=None):
+    """spd_varlen_attn_fwd_noalloc: the forward pass for callers that cannot
+    allocate. The caller passes every tensor (out, lse, and optionally a
+    one-element int32 device_status); the library uses its fixed scratch."""
+    _need_cuda(q, k, v, cu_seqlens, out, lse)
+    T, Hq, d = q.shape
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check("spd_varlen_attn_fwd_noalloc", load().spd_varlen_attn_fwd_noalloc(
+        _ptr(_as_u16(q)), _ptr(_as_u16(k)), _ptr(_as_u16(v)), _ptr(cu_seqlens), int(num_segs), T, int(max_seqlen),
+        Hq, k.shape[1], d, scale, _ptr(out), _ptr(lse), _ptr(device_status), _stream(stream)))
+    return out, lse
