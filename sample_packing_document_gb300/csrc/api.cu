@@ -86,6 +86,22 @@ int make_map(CUtensorMap *m, const void *base, int64_t T, int H, int D)
     return r == CUDA_SUCCESS ? SPD_OK : SPD_ERR_CUDA;
 }
 
+// Tensor map over the fp32 dQ accumulator laid out [Hq * D / 32][T][32]:
+// dims (32, T, Hq * D / 32), box (32, 32, 1), 128-byte swizzle. Rows past T
+// are clipped by the reduce.
+int make_dqacc_map(CUtensorMap *m, float *base, int64_t T, int Hq, int D)
+{
+    EncodeTiled f = encode_fn();
+    if (!f) return SPD_ERR_CUDA;
+    cuuint64_t dims[3] = {32, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(Hq) * (D / 32)};
+    cuuint64_t strides[2] = {32 * 4, static_cast<cuuint64_t>(T) * 32 * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SPD_OK : SPD_ERR_CUDA;
+}
+
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? SPD_OK : SPD_ERR_CUDA; }
 
 int check_attn_shape(int64_t T, int32_t num_segs, int Hq, int Hkv, int D)
@@ -313,6 +329,7 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.lse = lse;
     a.delta = reinterpret_cast<float *>(base + bwd_delta_off(total_tokens, num_segs));
     a.dq_acc = reinterpret_cast<float *>(base + bwd_acc_off(total_tokens, num_segs, Hq));
+    if ((rc = make_dqacc_map(&a.tm_dqacc, a.dq_acc, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;

@@ -10,30 +10,38 @@
 //
 // Three launches:
 //   bwd_pre_kernel   D_i = rowsum(dO * O) (fp32) and zeroes the fp32 dQ
-//                    accumulator [Hq, T, d].
+//                    accumulator, laid out [Hq][d / 32][T][32].
 //   attn_bwd_kernel  one CTA per (128-row kv tile, kv head): K, V stay in shared
 //                    memory; the CTA walks every (q head of the group, q tile
 //                    from the diagonal to the segment end). Per step, five
 //                    tcgen05 MMAs with fp32 accumulation in TMEM:
-//                      S^T = K Q^T, dP^T = V dO^T        (TMEM, 128 x 128)
-//                      dV += P^T dO, dK += dS^T Q        (TMEM accumulators)
-//                      dQ_part = dS K                    (TMEM, then red.add to HBM)
+//                      S^T = K Q^T  (region A),  dP^T = V dO^T  (region B)
+//                      dV += P^T dO, dK += dS^T Q          (accumulators C, E)
+//                      dQ_part = dS K  (region B, once dP^T has been read;
+//                                       then TMA reduce-add into the HBM accumulator)
 //                    P^T and dS^T go through one bf16 shared-memory buffer; the
 //                    dQ MMA reads dS^T back as an M-major operand, so dS is
 //                    written once.
 //   bwd_dq_kernel    dq = scale * accumulator, in the output layout and type.
 //
-// Warp roles of attn_bwd_kernel (192 threads): warps 0-3 compute (thread t owns
-// kv row t = TMEM lane t for S^T / dP^T / dK / dV, and q row t for the dQ
-// readout), warp 4 TMA producer, warp 5 MMA issuer.
-// TMEM: S^T and then dQ [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d).
+// Issue order on the tensor pipe: dP(i), dV(i), dK(i), dQ(i), S(i+1), dP(i+1), ...
+// so each elementwise phase overlaps an MMA: the dQ(i) read-out runs beside
+// S(i+1), P(i+1) beside dP(i+1), dS(i+1) beside dV(i+1).
+//
+// Warp roles (320 threads): warps 0-7 compute, two warpgroups; thread (w, l)
+// owns TMEM lane 32 (w % 4) + l (kv row for S^T / dP^T / dK / dV, q row for
+// the dQ read-out) and warpgroup w / 4 owns one half of the columns. Warp 8 is
+// the TMA producer, warp 9 issues the MMAs.
+// TMEM: A = S^T [0,128), B = dP^T then dQ [128,256), C = dV [256,256+d),
+// E = dK [256+d, 256+2d).
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace spd {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kCompute = 256;        // compute threads (warps 0-7)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;
 constexpr int kQStages = 2;
@@ -49,8 +57,8 @@ struct BwdSmem {
     float delta[2][128];             // D of the step's q columns
     uint64_t kv_full;
     uint64_t q_full[kQStages], q_empty[kQStages], do_full[kQStages], do_empty[kQStages];
-    uint64_t s_full, dp_full, dp_free, p_full, dv_done, ds_full, pds_free, dq_full, dq_free;
-    uint64_t cols[2];                // the step's lse2 / delta written (128 arrivals)
+    uint64_t s_full, s_free, dp_full, p_full, dv_done, ds_full, dq_full, dq_free;
+    uint64_t cols[2];                // the step's lse2 / delta written
     uint64_t fin, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -78,19 +86,24 @@ __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float 
                  : "memory");
 }
 
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Writes one 128-column bf16 row (64 packed words) into a [128][128] tile of
-// two 128-byte-swizzled atoms.
-__device__ __forceinline__ void store_row_sw128(uint32_t tile_addr, int row, const uint32_t (&pk)[64])
+// Writes 64 bf16 values (32 packed words) of one row into one 128-byte-swizzled
+// [128 rows][64 cols] atom.
+__device__ __forceinline__ void store_half_row_sw128(uint32_t atom_addr, int row, const uint32_t (&pk)[32])
 {
-    const uint32_t base = tile_addr + row * 128;
+    const uint32_t base = atom_addr + row * 128;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const uint32_t addr = base + (c >> 3) * kAtom + (((c & 7) ^ (row & 7)) << 4);
-        st_shared_v4(addr, pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-    }
+    for (int c = 0; c < 8; ++c)
+        st_shared_v4(base + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
 // ------------------------------------------------------------------ preprocess
@@ -131,10 +144,13 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
         const int h = static_cast<int>(row % Hq);
         const long long hi = static_cast<long long>(h) * T + i;
         if (sub == 0) delta[hi] = acc;
-        float4 *z = reinterpret_cast<float4 *>(dq_acc + hi * D + sub * kPer);
-#pragma unroll
-        for (int c = 0; c < kPer / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    // zero the fp32 dQ accumulator (any layout: Hq * T * D floats)
+    float4 *z = reinterpret_cast<float4 *>(dq_acc);
+    const long long n4 = rows * (D / 4);
+    for (long long x = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; x < n4;
+         x += static_cast<long long>(gridDim.x) * blockDim.x)
+        z[x] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ dq convert
@@ -150,7 +166,10 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
         const int c8 = static_cast<int>(x % (D / 8));
         const long long i = row / Hq;
         const int h = static_cast<int>(row % Hq);
-        const float4 *src = reinterpret_cast<const float4 *>(dq_acc + (static_cast<long long>(h) * T + i) * D + c8 * 8);
+        // accumulator layout [h][d / 32][i][32]
+        const int dblk = c8 >> 2, din = (c8 & 3) * 8;
+        const float4 *src = reinterpret_cast<const float4 *>(
+            dq_acc + ((static_cast<long long>(h) * (D / 32) + dblk) * T + i) * 32 + din);
         float4 a = src[0], b = src[1];
         float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         if (grad_fp32) {
@@ -178,8 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         if (threadIdx.x == 0) set_status(a.status, kErrTimeout);
         return;
     }
-    const int tile_idx = blockIdx.x / a.Hkv;
-    const int g = blockIdx.x % a.Hkv;
+    // kv-head-major order: the CTAs of one kv head run together, so the Q / dO
+    // tiles they share and the dQ rows they add into stay in L2.
+    const int g = blockIdx.x / a.grid_tiles;
+    const int tile_idx = blockIdx.x % a.grid_tiles;
     if (tile_idx >= *a.tile_count) return;
     const Tile tl = a.tiles[tile_idx];
     const int group = a.Hq / a.Hkv;
@@ -192,31 +213,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(&sm.kv_full, 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&sm.q_full[s], 1);
-            mbar_init(&sm.q_empty[s], 1);
+            mbar_init(&sm.q_empty[s], kCompute / 32);
             mbar_init(&sm.do_full[s], 1);
             mbar_init(&sm.do_empty[s], 1);
         }
         mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.s_free, kCompute);
         mbar_init(&sm.dp_full, 1);
-        mbar_init(&sm.dp_free, 128);
-        mbar_init(&sm.p_full, 128);
+        mbar_init(&sm.p_full, kCompute);
         mbar_init(&sm.dv_done, 1);
-        mbar_init(&sm.ds_full, 128);
-        mbar_init(&sm.pds_free, 1);
+        mbar_init(&sm.ds_full, kCompute);
         mbar_init(&sm.dq_full, 1);
-        mbar_init(&sm.dq_free, 128);
-        mbar_init(&sm.cols[0], 128);
-        mbar_init(&sm.cols[1], 128);
+        mbar_init(&sm.dq_free, kCompute);
+        mbar_init(&sm.cols[0], kCompute);
+        mbar_init(&sm.cols[1], kCompute);
         mbar_init(&sm.fin, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&a.tm_q);
         tma_prefetch_desc(&a.tm_k);
         tma_prefetch_desc(&a.tm_v);
@@ -228,9 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
     constexpr uint32_t kTileBytes = 128 * D * 2;
-    constexpr uint32_t kDV = 256, kDK = 256 + D;
+    constexpr uint32_t kA = 0, kB = 128, kC = 256, kE = 256 + D;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
@@ -263,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_ss = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
@@ -271,31 +291,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             constexpr uint32_t id_mn = idesc_bf16(128, D, 1, 1);    // dQ
             const uint32_t k_addr = smem_u32(sm.k[0]), v_addr = smem_u32(sm.v[0]);
             const uint32_t pds_addr = smem_u32(sm.pds[0]);
-            int q_commits[kQStages] = {}, do_commits[kQStages] = {};
-            bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, a.status);
+            int do_commits[kQStages] = {};
+            auto issue_s = [&](int i) -> bool {  // S^T(i) = K Q(i)^T into A
+                const int st = i % kQStages;
+                if (!mbar_wait(&sm.q_full[st], (i / kQStages) & 1, abort_flag, a.status)) return false;
+                if (i > 0 && !mbar_wait(&sm.s_free, (i - 1) & 1, abort_flag, a.status)) return false;
+                tc_fence_after();
+                const uint32_t q_addr = smem_u32(sm.q[st][0]);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                    umma_bf16(tmem + kA, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
+                              id_ss, kk > 0 ? 1u : 0u);
+                }
+                umma_commit(&sm.s_full);
+                return true;
+            };
+            bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, a.status) && issue_s(0);
             for (int i = 0; ok && i < nsteps; ++i) {
                 const int st = i % kQStages, u = i / kQStages;
                 const uint32_t q_addr = smem_u32(sm.q[st][0]), do_addr = smem_u32(sm.dout[st][0]);
                 const uint32_t ph = i & 1, pph = (i - 1) & 1;
-                // S^T = K Q^T  (M = kv, N = q, K = d)
-                if (!mbar_wait(&sm.q_full[st], u & 1, abort_flag, a.status)) { ok = false; break; }
+                // dP^T(i) = V dO(i)^T into B, once dQ(i-1) has been read out of B
+                if (!mbar_wait(&sm.do_full[st], u & 1, abort_flag, a.status)) { ok = false; break; }
                 if (i > 0 && !mbar_wait(&sm.dq_free, pph, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    umma_bf16(tmem + 0, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
-                              id_ss, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&sm.s_full);
-                // dP^T = V dO^T
-                if (!mbar_wait(&sm.do_full[st], u & 1, abort_flag, a.status)) { ok = false; break; }
-                if (i > 0 && !mbar_wait(&sm.dp_free, pph, abort_flag, a.status)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    umma_bf16(tmem + 128, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
+                    umma_bf16(tmem + kB, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
                               id_ss, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&sm.dp_full);
@@ -304,92 +328,94 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 128 / 16; ++kk)
-                    umma_bf16(tmem + kDV, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                    umma_bf16(tmem + kC, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
                               sdesc_sw128(do_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&sm.dv_done);
                 umma_commit(&sm.do_empty[st]);
                 ++do_commits[st];
-                // dK += dS^T Q, dQ_part = dS K
+                // dK += dS^T Q (M = kv), dQ_part = dS K (M = q) into B
                 if (!mbar_wait(&sm.ds_full, ph, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 128 / 16; ++kk)
-                    umma_bf16(tmem + kDK, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                    umma_bf16(tmem + kE, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
                               sdesc_sw128(q_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < 128 / 16; ++kk)
-                    umma_bf16(tmem + 0, sdesc_sw128(pds_addr + kk * 2048, kAtom, 1024),
+                    umma_bf16(tmem + kB, sdesc_sw128(pds_addr + kk * 2048, kAtom, 1024),
                               sdesc_sw128(k_addr + kk * 2048, kAtom, 1024), id_mn, kk > 0 ? 1u : 0u);
-                umma_commit(&sm.pds_free);
-                umma_commit(&sm.q_empty[st]);
-                ++q_commits[st];
                 umma_commit(&sm.dq_full);
+                if (i + 1 < nsteps && !issue_s(i + 1)) { ok = false; break; }
             }
             umma_commit(&sm.fin);
             umma_commit(&sm.drain);
             wait_drain(&sm.drain, 0);
-            for (int s = 0; s < kQStages; ++s) {
-                if (q_commits[s] > 0) wait_drain(&sm.q_empty[s], (q_commits[s] - 1) & 1);
+            for (int s = 0; s < kQStages; ++s)
                 if (do_commits[s] > 0) wait_drain(&sm.do_empty[s], (do_commits[s] - 1) & 1);
-            }
         }
     } else {
         // ------------------------------------------------------------ compute
-        const int t = threadIdx.x;  // kv row (and q row for dQ) = TMEM lane
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t pds_addr = smem_u32(sm.pds[0]);
+        const int quarter = warp & 3, half = warp >> 2;
+        const int t = quarter * 32 + lane;                       // TMEM lane / row
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t col0 = half * 64;                         // this warpgroup's column half
+        const uint32_t atom_addr = smem_u32(sm.pds[half]);
         const float sl2 = a.scale_log2;
         const int kj = k0 + t;
+        const int ct = threadIdx.x & 127;                        // column whose terms this thread loads
         bool ok = true;
-        // prefetch the step's per-column terms
-        auto col_terms = [&](int i, float &l2, float &dd) {
+        auto col_term = [&](int i) -> float {
             const int h = g * group + i / nq;
-            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + t;
-            l2 = 0.f;
-            dd = 0.f;
-            if (qi < a.total_tokens) {
-                const size_t idx = static_cast<size_t>(h) * a.total_tokens + qi;
-                l2 = a.lse[idx] * 1.4426950408889634f;
-                dd = a.delta[idx];
-            }
+            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + ct;
+            if (qi >= a.total_tokens) return 0.f;
+            const size_t idx = static_cast<size_t>(h) * a.total_tokens + qi;
+            return half ? a.delta[idx] : a.lse[idx] * 1.4426950408889634f;
         };
-        float nl2, ndd;
-        col_terms(0, nl2, ndd);
+        float nxt = col_term(0);
         for (int i = 0; i < nsteps; ++i) {
             const int h = g * group + i / nq;
-            const int qt = tl.t + i % nq;
-            const int q0 = tl.seg_start + qt * kTile;
-            const uint32_t ph = i & 1, pph = (i - 1) & 1;
-            sm.lse2[i & 1][t] = nl2;
-            sm.delta[i & 1][t] = ndd;
+            const int q0 = tl.seg_start + (tl.t + i % nq) * kTile;
+            const uint32_t ph = i & 1;
+            (half ? sm.delta : sm.lse2)[i & 1][ct] = nxt;
             mbar_arrive(&sm.cols[i & 1]);
-            if (i + 1 < nsteps) col_terms(i + 1, nl2, ndd);
+            if (i + 1 < nsteps) nxt = col_term(i + 1);
             if (!warp_wait(&sm.cols[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-            const float *L2 = sm.lse2[i & 1];
-            const float *DD = sm.delta[i & 1];
-            // column c (q row q0 + c) is live for kv row kj iff kj <= q0 + c < seg_end
-            const int c_lo = kj - q0;                 // first live column
-            const int c_hi = tl.seg_end - q0;         // columns >= c_hi are past the segment
+            const float *L2 = sm.lse2[i & 1] + col0;
+            const float *DD = sm.delta[i & 1] + col0;
+            // column c of this half (q row q0 + col0 + c) is live for kv row kj iff kj <= q row < seg_end
+            const int c_lo = kj - q0 - static_cast<int>(col0);
+            const int c_hi = tl.seg_end - q0 - static_cast<int>(col0);
 
             // P^T = exp(S^T * scale - LSE)
             if (!warp_wait(&sm.s_full, ph, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
-            uint32_t s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld32(tmem + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+            uint32_t s[64];
+            tmem_ld32(tmem + lane_off + kA + col0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+            tmem_ld32(tmem + lane_off + kA + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
             tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&sm.s_free);
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
+            for (int c = 0; c < 64; ++c) {
                 float p = ex2(__uint_as_float(s[c]) * sl2 - L2[c]);
                 if (c < c_lo || c >= c_hi) p = 0.f;
                 s[c] = __float_as_uint(p);
             }
-            uint32_t pk[64];
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-            if (i > 0 && !warp_wait(&sm.pds_free, pph, abort_flag, a.status)) { ok = false; break; }
-            store_row_sw128(pds_addr, t, pk);
+            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
+            // The buffer is free once dK(i-1) / dQ(i-1) have read dS(i-1) (they
+            // completed before dq_full(i-1)) and the TMA engine has read the dQ(i-1)
+            // chunks staged in it and in the Q(i-1) stage; then that Q stage goes
+            // back to the producer.
+            if (i > 0) {
+                if (lane == 0) {
+                    bulk_wait_group_read0();
+                    mbar_arrive(&sm.q_empty[(i - 1) % kQStages]);
+                }
+                __syncwarp();
+            }
+            store_half_row_sw128(atom_addr, t, pk);
             fence_proxy_async_smem();
             mbar_arrive(&sm.p_full);
 
@@ -397,9 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             if (!warp_wait(&sm.dp_full, ph, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t dp[32];
-                tmem_ld32(tmem + lane_off + 128 + c * 32, dp);
+                tmem_ld32(tmem + lane_off + kB + col0 + c * 32, dp);
                 tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -409,46 +435,60 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     pk[c * 16 + e] = pack_bf16x2(d0, d1);
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&sm.dp_free);
             if (!warp_wait(&sm.dv_done, ph, abort_flag, a.status)) { ok = false; break; }
-            store_row_sw128(pds_addr, t, pk);
+            store_half_row_sw128(atom_addr, t, pk);
             fence_proxy_async_smem();
+            tc_fence_before();
             mbar_arrive(&sm.ds_full);
 
-            // dQ rows q0 + t: accumulate into HBM
+            // dQ rows q0 + t, d columns of this half: add into the HBM accumulator.
+            // Each warp stages [32 rows][32 cols] fp32 chunks in the 128-byte-swizzled
+            // layout -- chunk 0 in its slice of the P / dS buffer, chunk 1 in its
+            // slice of the Q(i) stage (both free: dK(i) and dQ(i) completed) -- and
+            // hands them to the TMA engine as reduce-adds that run in the
+            // background; nothing waits for them until those buffers are reused.
+            // Rows past the segment carry exact zeros.
             if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
-            const int qrow = q0 + t;
-            float *dst = a.dq_acc + (static_cast<size_t>(h) * a.total_tokens + qrow) * D;
-            const bool live = qrow < tl.seg_end;
+            {
+                const int st = i % kQStages;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + c * 32, v);
-                tmem_wait_ld();
-                if (live) {
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_off + kB + (D / 2) * half + c * 32, v);
+                    tmem_wait_ld();
+                    const uint8_t *stage = (c == 0 ? sm.pds[0] : sm.q[st][0]) + warp * 4096;
+                    const uint32_t stage_addr = smem_u32(stage);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        red_add_v4(dst + c * 32 + 4 * e, __uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                   __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                        st_shared_v4(stage_addr + lane * 128 + ((e ^ (lane & 7)) << 4), v[4 * e], v[4 * e + 1],
+                                     v[4 * e + 2], v[4 * e + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && q0 + quarter * 32 < tl.seg_end) {  // skip a chunk of padding rows only
+                        const int dblk = h * (D / 32) + (D / 64) * half + c;
+                        tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, dblk);
+                    }
                 }
+                if (lane == 0) bulk_commit_group();
             }
             tc_fence_before();
             mbar_arrive(&sm.dq_free);
         }
-        // dK, dV rows of this tile
+        if (lane == 0) bulk_wait_group0();     // every reduce of this warp has landed
+        __syncwarp();
+        // dK, dV rows of this tile, d columns of this half
         if (ok && warp_wait(&sm.fin, 0, abort_flag, a.status)) {
             tc_fence_after();
             const bool live = kj < tl.seg_end;
-            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + g) * D;
+            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + g) * D + (D / 2) * half;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which ? kDK : kDV;
+                const uint32_t col = (which ? kE : kC) + (D / 2) * half;
                 const float mul = which ? a.scale : 1.f;
                 void *base = which ? a.dk : a.dv;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < D / 64; ++c) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_off + col + c * 32, v);
                     tmem_wait_ld();
@@ -476,8 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 9) tmem_dealloc(tmem, kTmemCols);
 }
+
 
 template <int D>
 cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t stream)
@@ -496,11 +537,13 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t 
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    AttnBwdArgs a2 = a;
+    a2.grid_tiles = static_cast<int32_t>(grid_tiles);
     const int64_t grid = grid_tiles * a.Hkv;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (grid > 0) {
         prof_begin(kProfAttnBwd, stream);
-        attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+        attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a2);
         prof_end(kProfAttnBwd, stream);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;

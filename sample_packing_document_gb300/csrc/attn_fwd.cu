@@ -68,8 +68,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (*reinterpret_cast<volatile int *>(a.status) != 0) return;
-    const int tile_idx = blockIdx.x / a.Hq;
-    const int h = blockIdx.x % a.Hq;
+    // Head-major order: the CTAs of one head (and the heads of one kv group)
+    // run together, so the K / V tiles they share stay in L2; inside a head the
+    // work list is longest-first.
+    const int h = blockIdx.x / a.grid_tiles;
+    const int tile_idx = blockIdx.x % a.grid_tiles;
     if (tile_idx >= *a.tile_count) return;
     const Tile tl = a.tiles[tile_idx];
     const int q0 = tl.seg_start + tl.t * kTile;
@@ -302,11 +305,13 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, int64_t grid_tiles, cudaStream_t 
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    AttnFwdArgs a2 = a;
+    a2.grid_tiles = static_cast<int32_t>(grid_tiles);
     const int64_t grid = grid_tiles * a.Hq;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     prof_begin(kProfAttnFwd, stream);
-    attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+    attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a2);
     prof_end(kProfAttnFwd, stream);
     return cudaGetLastError();
 }

@@ -101,7 +101,8 @@ struct AttnFwdArgs {
     int *status;
     int32_t total_tokens;
     int32_t Hq, Hkv;
-    float scale_log2;  // softmax_scale * log2(e)
+    int32_t grid_tiles;  // tile slots per head in the grid (blockIdx = head * grid_tiles + tile)
+    float scale_log2;    // softmax_scale * log2(e)
     float scale;
 };
 
@@ -110,10 +111,11 @@ cudaError_t launch_attn_fwd(const AttnFwdArgs &a, int head_dim, int64_t grid_til
 
 struct AttnBwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
+    CUtensorMap tm_dqacc;  // fp32 dQ accumulator as [Hq * d / 32][T][32]
     const uint16_t *out;
     const uint16_t *dout;
     const float *lse;
-    float *dq_acc;   // [Hq, total_tokens, head_dim] fp32
+    float *dq_acc;   // fp32 [Hq][head_dim / 32][total_tokens][32] (d-blocked)
     float *delta;    // [Hq, total_tokens] fp32
     void *dq, *dk, *dv;
     int grad_fp32;
@@ -122,6 +124,7 @@ struct AttnBwdArgs {
     int *status;
     int32_t total_tokens;
     int32_t Hq, Hkv;
+    int32_t grid_tiles;  // tile slots per kv head in the grid (blockIdx = kv head * grid_tiles + tile)
     float scale_log2;
     float scale;
 };
