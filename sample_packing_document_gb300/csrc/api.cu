@@ -272,7 +272,7 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     if (rc != SPD_OK) return rc;
     if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
 
-    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, ws, s));
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, 2, ws, s));
     if (rc != SPD_OK) return rc;
     AttnFwdArgs a = {};
     if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
@@ -289,7 +289,7 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.Hkv = Hkv;
     a.scale = softmax_scale;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    return cuda_rc(launch_attn_fwd(a, head_dim, max_tiles(total_tokens, num_segs), s));
+    return cuda_rc(launch_attn_fwd(a, head_dim, (total_tokens + 2 * kTile - 1) / (2 * kTile) + num_segs, s));
 }
 
 int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *out,
@@ -316,7 +316,7 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     if (rc != SPD_OK) return rc;
     if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
 
-    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 1, ws, s));
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 1, 1, ws, s));
     if (rc != SPD_OK) return rc;
     AttnBwdArgs a = {};
     if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;

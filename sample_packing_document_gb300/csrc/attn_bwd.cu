@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             mbar_arrive(&sm.cols[i & 1]);
             if (i + 1 < nsteps) nxt = col_term(i + 1);
             if (!warp_wait(&sm.cols[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+
             const float *L2 = sm.lse2[i & 1] + col0;
             const float *DD = sm.delta[i & 1] + col0;
             // column c of this half (q row q0 + col0 + c) is live for kv row kj iff kj <= q row < seg_end
@@ -395,11 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(&sm.s_free);
+            if (c_lo <= 0 && c_hi >= 64) {       // every column of this half is live
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float p = ex2(__uint_as_float(s[c]) * sl2 - L2[c]);
-                if (c < c_lo || c >= c_hi) p = 0.f;
-                s[c] = __float_as_uint(p);
+                for (int c = 0; c < 64; ++c) s[c] = __float_as_uint(ex2(__uint_as_float(s[c]) * sl2 - L2[c]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    float p = ex2(__uint_as_float(s[c]) * sl2 - L2[c]);
+                    if (c < c_lo || c >= c_hi) p = 0.f;
+                    s[c] = __float_as_uint(p);
+                }
             }
             uint32_t pk[32];
 #pragma unroll
@@ -407,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             // The buffer is free once dK(i-1) / dQ(i-1) have read dS(i-1) (they
             // completed before dq_full(i-1)) and the TMA engine has read the dQ(i-1)
             // chunks staged in it and in the Q(i-1) stage; then that Q stage goes
-            // back to the producer.
+            // back to the producer. Waiting here rather than earlier leaves the
+            // engine the whole P computation to read them.
             if (i > 0) {
                 if (lane == 0) {
                     bulk_wait_group_read0();

@@ -85,10 +85,12 @@ inline int64_t max_tiles(int64_t total_tokens, int64_t num_segs)
 }
 
 // Builds the work list into the workspace (after the header): validates
-// cu_seqlens (status SPD_ERR_BAD_SEQLENS on failure) and writes the tile count
-// to ws[1]. order: 0 = forward costs (t + 1), 1 = backward costs (n - t).
+// cu_seqlens (status SPD_ERR_BAD_SEQLENS on failure) and writes the unit count
+// to ws[1]. order: 0 = forward costs, 1 = backward costs (n - t). unit: tiles
+// per work unit (2 = a pair of consecutive q tiles, forward only); Tile.t is
+// the unit's first tile.
 cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
-                            int order, void *ws, cudaStream_t stream);
+                            int order, int unit, void *ws, cudaStream_t stream);
 size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs);
 
 // ---------------------------------------------------------------- attention

@@ -10,8 +10,10 @@
 // (longest-processing-time first) lets the many short tiles fill in behind
 // the few long ones when documents are very uneven.
 //
-// One CTA: validates cu_seqlens, counts tiles per segment (exclusive scan ->
-// tile offsets), then a counting sort by cost over all tiles in parallel.
+// One CTA: validates cu_seqlens, counts work units per segment (exclusive scan
+// -> unit offsets), then a counting sort by cost over all units in parallel. A
+// unit is one tile (backward, and forward with unit = 1) or two consecutive q
+// tiles of a segment that one forward CTA computes together (unit = 2).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -49,7 +51,7 @@ __device__ long long block_scan_excl(long long v, long long *total, long long *s
 }
 
 __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, int32_t nsegs,
-                                                            int64_t T, int order, int *status,
+                                                            int64_t T, int order, int unit, int *status,
                                                             int32_t *count, Tile *tiles,
                                                             int32_t *tile_off)
 {
@@ -73,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
         if (s < nsegs) {
             int a = cu[s], b = cu[s + 1];
             if (b <= a) bad = true;
-            else n = (b - a + kTile - 1) / kTile;
+            else n = ((b - a + kTile - 1) / kTile + unit - 1) / unit;
         }
         long long tot;
         long long e = block_scan_excl(n, &tot, sh) + carry;
@@ -100,9 +102,10 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
             else hi = mid;
         }
         s = lo;
-        t = i - tile_off[s];
-        n = tile_off[s + 1] - tile_off[s];
-        cost = order ? n - t : t + 1;
+        t = (i - tile_off[s]) * unit;                       // first tile of the unit
+        n = (cu[s + 1] - cu[s] + kTile - 1) / kTile;        // tiles of the segment
+        if (order) cost = n - t;                            // backward: q tiles t .. n-1
+        else cost = (t + 1) + (unit > 1 && t + 1 < n ? t + 2 : 0);  // forward: kv tiles of each q tile
     };
 
     for (int i = tid; i < ntiles; i += kThreads) {
@@ -144,7 +147,7 @@ size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs)
 }
 
 cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
-                            int order, void *ws, cudaStream_t stream)
+                            int order, int unit, void *ws, cudaStream_t stream)
 {
     char *base = reinterpret_cast<char *>(ws);
     int *status = reinterpret_cast<int *>(base);
@@ -152,7 +155,7 @@ cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t
     Tile *tiles = reinterpret_cast<Tile *>(base + kWsHeader);
     int32_t *tile_off = reinterpret_cast<int32_t *>(
         base + kWsHeader + align_up(sizeof(Tile) * static_cast<size_t>(max_tiles(total_tokens, num_segs)), 256));
-    schedule_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_segs, total_tokens, order, status,
+    schedule_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_segs, total_tokens, order, unit, status,
                                                 count, tiles, tile_off);
     return cudaGetLastError();
 }
