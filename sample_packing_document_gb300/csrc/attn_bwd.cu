@@ -15,33 +15,35 @@
 //                    memory; the CTA walks every (q head of the group, q tile
 //                    from the diagonal to the segment end). Per step, five
 //                    tcgen05 MMAs with fp32 accumulation in TMEM:
-//                      S^T = K Q^T  (region A),  dP^T = V dO^T  (region B)
-//                      dV += P^T dO, dK += dS^T Q          (accumulators C, E)
-//                      dQ_part = dS K  (region B, once dP^T has been read;
-//                                       then TMA reduce-add into the HBM accumulator)
-//                    P^T and dS^T go through one bf16 shared-memory buffer; the
-//                    dQ MMA reads dS^T back as an M-major operand, so dS is
-//                    written once.
+//                      S^T = K Q^T           region A (P^T is then written over it, bf16)
+//                      dP^T = V dO^T         region B
+//                      dV += P^T dO          region C (P^T read from TMEM)
+//                      dK += dS^T Q          region E (dS^T from shared memory)
+//                      dQ_part = dS K        region B (once dP^T has been read), then
+//                                            TMA reduce-add into the HBM accumulator.
 //   bwd_dq_kernel    dq = scale * accumulator, in the output layout and type.
 //
-// Issue order on the tensor pipe: dP(i), dV(i), dK(i), dQ(i), S(i+1), dP(i+1), ...
-// so each elementwise phase overlaps an MMA: the dQ(i) read-out runs beside
-// S(i+1), P(i+1) beside dP(i+1), dS(i+1) beside dV(i+1).
-//
-// Warp roles (320 threads): warps 0-7 compute, two warpgroups; thread (w, l)
-// owns TMEM lane 32 (w % 4) + l (kv row for S^T / dP^T / dK / dV, q row for
-// the dQ read-out) and warpgroup w / 4 owns one half of the columns. Warp 8 is
-// the TMA producer, warp 9 issues the MMAs.
-// TMEM: A = S^T [0,128), B = dP^T then dQ [128,256), C = dV [256,256+d),
-// E = dK [256+d, 256+2d).
+// Warp roles (576 threads). Warp w works on TMEM lanes 32 (w % 4) .. +31 (kv
+// rows; q rows for the dQ read-out) and on one half of the columns:
+//   warps 0-7   "P": P^T(i) = exp(S^T(i) * scale - LSE) from region A, written
+//               back into it as bf16 (the P^T columns of a half sit in the first
+//               half of that half's S^T columns); then one 32 x 32 chunk of the
+//               dQ(i) read-out, staged in the spent Q(i) stage, and its reduce-add.
+//   warps 8-15  "dS": dS^T(i) = P^T(i) (dP^T(i) - D) into shared memory, then one
+//               chunk of the dQ(i) read-out, staged in the dS buffer; at the end
+//               the dK / dV stores.
+//   warp 16     TMA producer; warp 17 issues the MMAs in the order
+//              dV(i), dK(i), dQ(i), S(i+1), dP(i+1), dV(i+1), ...
+// so P(i+1) is computed while dK(i) / dQ(i) run, dS(i) while dV(i) runs, and the
+// dQ(i) read-out while S(i+1) runs.
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace spd {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kCompute = 256;        // compute threads (warps 0-7)
+constexpr int kThreads = 576;        // 16 compute warps + producer + MMA issuer
+constexpr int kPWarps = 8, kDsWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;
 constexpr int kQStages = 2;
@@ -52,13 +54,13 @@ struct BwdSmem {
     uint8_t v[D / 64][kAtom];
     uint8_t q[kQStages][D / 64][kAtom];
     uint8_t dout[kQStages][D / 64][kAtom];
-    uint8_t pds[2][kAtom];           // P^T, then dS^T: [128 kv rows][128 q cols]
+    uint8_t ds[2][kAtom];            // dS^T: [128 kv rows][128 q cols]
     float lse2[2][128];              // LSE * log2(e) of the step's q columns
     float delta[2][128];             // D of the step's q columns
     uint64_t kv_full;
     uint64_t q_full[kQStages], q_empty[kQStages], do_full[kQStages], do_empty[kQStages];
-    uint64_t s_full, s_free, dp_full, p_full, dv_done, ds_full, dq_full, dq_free;
-    uint64_t cols[2];                // the step's lse2 / delta written
+    uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free;
+    uint64_t cols_l[2], cols_d[2];   // the step's lse2 / delta written
     uint64_t fin, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -79,32 +81,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, w);
 }
 
-__device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d)
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, bf16) sits in TMEM, one row per
+// lane, two K elements per 32-bit column.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Writes 64 bf16 values (32 packed words) of one row into one 128-byte-swizzled
-// [128 rows][64 cols] atom.
-__device__ __forceinline__ void store_half_row_sw128(uint32_t atom_addr, int row, const uint32_t (&pk)[32])
-{
-    const uint32_t base = atom_addr + row * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        st_shared_v4(base + ((c ^ (row & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-}
 
 // ------------------------------------------------------------------ preprocess
 template <int D>
@@ -213,30 +205,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(&sm.kv_full, 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&sm.q_full[s], 1);
-            mbar_init(&sm.q_empty[s], kCompute / 32);
+            mbar_init(&sm.q_empty[s], 4 * (D / 64));  // the P warps that stage dQ there, once it is read
             mbar_init(&sm.do_full[s], 1);
             mbar_init(&sm.do_empty[s], 1);
         }
         mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_free, kCompute);
         mbar_init(&sm.dp_full, 1);
-        mbar_init(&sm.p_full, kCompute);
-        mbar_init(&sm.dv_done, 1);
-        mbar_init(&sm.ds_full, kCompute);
+        mbar_init(&sm.p_full, 32 * kPWarps);
+        mbar_init(&sm.ds_full, 32 * kDsWarps);
         mbar_init(&sm.dq_full, 1);
-        mbar_init(&sm.dq_free, kCompute);
-        mbar_init(&sm.cols[0], kCompute);
-        mbar_init(&sm.cols[1], kCompute);
+        mbar_init(&sm.dq_free, 32 * (kPWarps + kDsWarps));
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.cols_l[b], 128);
+            mbar_init(&sm.cols_d[b], 128);
+        }
         mbar_init(&sm.fin, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 17) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == 16 && lane == 0) {
         tma_prefetch_desc(&a.tm_q);
         tma_prefetch_desc(&a.tm_k);
         tma_prefetch_desc(&a.tm_v);
@@ -250,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     constexpr uint32_t kTileBytes = 128 * D * 2;
     constexpr uint32_t kA = 0, kB = 128, kC = 256, kE = 256 + D;
 
-    if (warp == 8) {
+    if (warp == 16) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
@@ -283,19 +275,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 17) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t id_ss = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
-            constexpr uint32_t id_kn = idesc_bf16(128, D, 0, 1);    // dV, dK
+            constexpr uint32_t id_kn = idesc_bf16(128, D, 0, 1);    // dV (A in TMEM), dK
             constexpr uint32_t id_mn = idesc_bf16(128, D, 1, 1);    // dQ
             const uint32_t k_addr = smem_u32(sm.k[0]), v_addr = smem_u32(sm.v[0]);
-            const uint32_t pds_addr = smem_u32(sm.pds[0]);
+            const uint32_t ds_addr = smem_u32(sm.ds[0]);
             int do_commits[kQStages] = {};
-            auto issue_s = [&](int i) -> bool {  // S^T(i) = K Q(i)^T into A
+            auto issue_s = [&](int i) -> bool {   // S^T(i) = K Q(i)^T into A
                 const int st = i % kQStages;
                 if (!mbar_wait(&sm.q_full[st], (i / kQStages) & 1, abort_flag, a.status)) return false;
-                if (i > 0 && !mbar_wait(&sm.s_free, (i - 1) & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
                 const uint32_t q_addr = smem_u32(sm.q[st][0]);
 #pragma unroll
@@ -307,15 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 umma_commit(&sm.s_full);
                 return true;
             };
-            bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, a.status) && issue_s(0);
-            for (int i = 0; ok && i < nsteps; ++i) {
-                const int st = i % kQStages, u = i / kQStages;
-                const uint32_t q_addr = smem_u32(sm.q[st][0]), do_addr = smem_u32(sm.dout[st][0]);
-                const uint32_t ph = i & 1, pph = (i - 1) & 1;
-                // dP^T(i) = V dO(i)^T into B, once dQ(i-1) has been read out of B
-                if (!mbar_wait(&sm.do_full[st], u & 1, abort_flag, a.status)) { ok = false; break; }
-                if (i > 0 && !mbar_wait(&sm.dq_free, pph, abort_flag, a.status)) { ok = false; break; }
+            auto issue_dp = [&](int i) -> bool {  // dP^T(i) = V dO(i)^T into B, once dQ(i-1) left B
+                const int st = i % kQStages;
+                if (!mbar_wait(&sm.do_full[st], (i / kQStages) & 1, abort_flag, a.status)) return false;
+                if (i > 0 && !mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
+                const uint32_t do_addr = smem_u32(sm.dout[st][0]);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
@@ -323,29 +311,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                               id_ss, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&sm.dp_full);
-                // dV += P^T dO  (M = kv, N = d, K = q)
+                return true;
+            };
+            bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, a.status) && issue_s(0) && issue_dp(0);
+            for (int i = 0; ok && i < nsteps; ++i) {
+                const int st = i % kQStages;
+                const uint32_t ph = i & 1;
+                // dV += P^T(i) dO(i): P^T in TMEM over S^T (M = kv, K = q), dO MN-major
                 if (!mbar_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
+                {
+                    const uint32_t do_addr = smem_u32(sm.dout[st][0]);
 #pragma unroll
-                for (int kk = 0; kk < 128 / 16; ++kk)
-                    umma_bf16(tmem + kC, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                              sdesc_sw128(do_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&sm.dv_done);
+                    for (int kk = 0; kk < 128 / 16; ++kk)
+                        // P^T q columns 16kk .. 16kk+15 sit at TMEM column 64 (kk / 4) + 8 (kk % 4)
+                        umma_bf16_ts(tmem + kC, tmem + kA + (kk >> 2) * 64 + (kk & 3) * 8,
+                                     sdesc_sw128(do_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
+                }
                 umma_commit(&sm.do_empty[st]);
                 ++do_commits[st];
-                // dK += dS^T Q (M = kv), dQ_part = dS K (M = q) into B
+                // dK += dS^T Q(i) (M = kv), dQ_part = dS K (M = q) into B
                 if (!mbar_wait(&sm.ds_full, ph, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
+                {
+                    const uint32_t q_addr = smem_u32(sm.q[st][0]);
 #pragma unroll
-                for (int kk = 0; kk < 128 / 16; ++kk)
-                    umma_bf16(tmem + kE, sdesc_sw128(pds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                              sdesc_sw128(q_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 128 / 16; ++kk)
+                        umma_bf16(tmem + kE, sdesc_sw128(ds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                                  sdesc_sw128(q_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < 128 / 16; ++kk)
-                    umma_bf16(tmem + kB, sdesc_sw128(pds_addr + kk * 2048, kAtom, 1024),
-                              sdesc_sw128(k_addr + kk * 2048, kAtom, 1024), id_mn, kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < 128 / 16; ++kk)
+                        umma_bf16(tmem + kB, sdesc_sw128(ds_addr + kk * 2048, kAtom, 1024),
+                                  sdesc_sw128(k_addr + kk * 2048, kAtom, 1024), id_mn, kk > 0 ? 1u : 0u);
+                }
                 umma_commit(&sm.dq_full);
-                if (i + 1 < nsteps && !issue_s(i + 1)) { ok = false; break; }
+                // next step: S^T(i+1) over P^T(i) (dV(i) ran before it and the dS warps
+                // read P^T(i) before ds_full(i)), then dP^T(i+1)
+                if (i + 1 < nsteps && !(issue_s(i + 1) && issue_dp(i + 1))) { ok = false; break; }
             }
             umma_commit(&sm.fin);
             umma_commit(&sm.drain);
@@ -353,145 +355,208 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             for (int s = 0; s < kQStages; ++s)
                 if (do_commits[s] > 0) wait_drain(&sm.do_empty[s], (do_commits[s] - 1) & 1);
         }
-    } else {
-        // ------------------------------------------------------------ compute
+    } else if (warp < kPWarps) {
+        // ------------------------------------------------------------ P warps
         const int quarter = warp & 3, half = warp >> 2;
-        const int t = quarter * 32 + lane;                       // TMEM lane / row
+        const int t = quarter * 32 + lane;                        // kv row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t col0 = half * 64;                         // this warpgroup's column half
-        const uint32_t atom_addr = smem_u32(sm.pds[half]);
+        const int col0 = half * 64;                               // this warp's 64 q columns
         const float sl2 = a.scale_log2;
         const int kj = k0 + t;
-        const int ct = threadIdx.x & 127;                        // column whose terms this thread loads
+        const bool loader = half == 0;                            // loads the step's LSE column t
+        const int my_chunk = half;                                // dQ read-out chunk (d columns 32c..)
+        const bool reads_out = my_chunk < D / 64;
         bool ok = true;
         auto col_term = [&](int i) -> float {
             const int h = g * group + i / nq;
-            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + ct;
+            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + t;
             if (qi >= a.total_tokens) return 0.f;
-            const size_t idx = static_cast<size_t>(h) * a.total_tokens + qi;
-            return half ? a.delta[idx] : a.lse[idx] * 1.4426950408889634f;
+            return a.lse[static_cast<size_t>(h) * a.total_tokens + qi] * 1.4426950408889634f;
         };
-        float nxt = col_term(0);
+        float nxt = loader ? col_term(0) : 0.f;
         for (int i = 0; i < nsteps; ++i) {
             const int h = g * group + i / nq;
             const int q0 = tl.seg_start + (tl.t + i % nq) * kTile;
-            const uint32_t ph = i & 1;
-            (half ? sm.delta : sm.lse2)[i & 1][ct] = nxt;
-            mbar_arrive(&sm.cols[i & 1]);
-            if (i + 1 < nsteps) nxt = col_term(i + 1);
-            if (!warp_wait(&sm.cols[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-
-            const float *L2 = sm.lse2[i & 1] + col0;
-            const float *DD = sm.delta[i & 1] + col0;
-            // column c of this half (q row q0 + col0 + c) is live for kv row kj iff kj <= q row < seg_end
-            const int c_lo = kj - q0 - static_cast<int>(col0);
-            const int c_hi = tl.seg_end - q0 - static_cast<int>(col0);
-
-            // P^T = exp(S^T * scale - LSE)
-            if (!warp_wait(&sm.s_full, ph, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            uint32_t s[64];
-            tmem_ld32(tmem + lane_off + kA + col0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld32(tmem + lane_off + kA + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&sm.s_free);
-            if (c_lo <= 0 && c_hi >= 64) {       // every column of this half is live
-#pragma unroll
-                for (int c = 0; c < 64; ++c) s[c] = __float_as_uint(ex2(__uint_as_float(s[c]) * sl2 - L2[c]));
-            } else {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    float p = ex2(__uint_as_float(s[c]) * sl2 - L2[c]);
-                    if (c < c_lo || c >= c_hi) p = 0.f;
-                    s[c] = __float_as_uint(p);
-                }
+            if (loader) {
+                sm.lse2[i & 1][t] = nxt;
+                mbar_arrive(&sm.cols_l[i & 1]);
+                if (i + 1 < nsteps) nxt = col_term(i + 1);
             }
-            uint32_t pk[32];
+            if (!warp_wait(&sm.cols_l[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            const float *L2 = sm.lse2[i & 1] + col0;
+            // column col0 + c (q row q0 + col0 + c) is live for kv row kj iff kj <= q row < seg_end
+            const int c_lo = kj - q0 - col0, c_hi = tl.seg_end - q0 - col0;
+            const bool full = c_lo <= 0 && c_hi >= 64;
+            if (!warp_wait(&sm.s_full, i & 1, abort_flag, a.status)) { ok = false; break; }
+            tc_fence_after();
+            // P^T columns col0 + 32c .. +31 (bf16 pairs) go to TMEM columns col0 + 16c ..
+            // +15, inside the S^T columns this warp has already read itself.
 #pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-            // The buffer is free once dK(i-1) / dQ(i-1) have read dS(i-1) (they
-            // completed before dq_full(i-1)) and the TMA engine has read the dQ(i-1)
-            // chunks staged in it and in the Q(i-1) stage; then that Q stage goes
-            // back to the producer. Waiting here rather than earlier leaves the
-            // engine the whole P computation to read them.
-            if (i > 0) {
+            for (int c = 0; c < 2; ++c) {
+                uint32_t sv[32];
+                tmem_ld32(tmem + lane_off + kA + col0 + c * 32, sv);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int col = c * 32 + 2 * e;
+                    float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - L2[col]);
+                    float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - L2[col + 1]);
+                    if (!full) {
+                        if (col < c_lo || col >= c_hi) p0 = 0.f;
+                        if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                    }
+                    pk[e] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16(tmem + lane_off + kA + col0 + c * 16, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full);
+            // The Q(i-1) stage held this warp's staged dQ(i-1) chunk: once the TMA
+            // engine has read it (it had the whole P computation to do so) the
+            // stage goes back to the producer.
+            if (i > 0 && reads_out) {
                 if (lane == 0) {
                     bulk_wait_group_read0();
                     mbar_arrive(&sm.q_empty[(i - 1) % kQStages]);
                 }
                 __syncwarp();
             }
-            store_half_row_sw128(atom_addr, t, pk);
-            fence_proxy_async_smem();
-            mbar_arrive(&sm.p_full);
-
-            // dS^T = P^T * (dP^T - D)
-            if (!warp_wait(&sm.dp_full, ph, abort_flag, a.status)) { ok = false; break; }
+            // dQ(i) read-out of one [32 rows][32 cols] chunk, staged in this warp's
+            // slice of the Q(i) stage (free once dK(i) completed) in the 128-byte-
+            // swizzled layout and added by the TMA engine in the background.
+            if (!warp_wait(&sm.dq_full, i & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t dp[32];
-                tmem_ld32(tmem + lane_off + kB + col0 + c * 32, dp);
+            if (reads_out) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + kB + my_chunk * 32, v);
                 tmem_wait_ld();
+                const uint8_t *stage = sm.q[i % kQStages][0] + (quarter + 4 * my_chunk) * 4096;
+                const uint32_t stage_addr = smem_u32(stage);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c0 = c * 32 + 2 * e;
-                    float d0 = __uint_as_float(s[c0]) * (__uint_as_float(dp[2 * e]) - DD[c0]);
-                    float d1 = __uint_as_float(s[c0 + 1]) * (__uint_as_float(dp[2 * e + 1]) - DD[c0 + 1]);
-                    pk[c * 16 + e] = pack_bf16x2(d0, d1);
+                for (int e = 0; e < 8; ++e)
+                    st_shared_v4(stage_addr + lane * 128 + ((e ^ (lane & 7)) << 4), v[4 * e], v[4 * e + 1],
+                                 v[4 * e + 2], v[4 * e + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (q0 + quarter * 32 < tl.seg_end)   // skip a chunk of padding rows only
+                        tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, h * (D / 32) + my_chunk);
+                    bulk_commit_group();
                 }
-            }
-            if (!warp_wait(&sm.dv_done, ph, abort_flag, a.status)) { ok = false; break; }
-            store_half_row_sw128(atom_addr, t, pk);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&sm.ds_full);
-
-            // dQ rows q0 + t, d columns of this half: add into the HBM accumulator.
-            // Each warp stages [32 rows][32 cols] fp32 chunks in the 128-byte-swizzled
-            // layout -- chunk 0 in its slice of the P / dS buffer, chunk 1 in its
-            // slice of the Q(i) stage (both free: dK(i) and dQ(i) completed) -- and
-            // hands them to the TMA engine as reduce-adds that run in the
-            // background; nothing waits for them until those buffers are reused.
-            // Rows past the segment carry exact zeros.
-            if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            {
-                const int st = i % kQStages;
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + kB + (D / 2) * half + c * 32, v);
-                    tmem_wait_ld();
-                    const uint8_t *stage = (c == 0 ? sm.pds[0] : sm.q[st][0]) + warp * 4096;
-                    const uint32_t stage_addr = smem_u32(stage);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        st_shared_v4(stage_addr + lane * 128 + ((e ^ (lane & 7)) << 4), v[4 * e], v[4 * e + 1],
-                                     v[4 * e + 2], v[4 * e + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && q0 + quarter * 32 < tl.seg_end) {  // skip a chunk of padding rows only
-                        const int dblk = h * (D / 32) + (D / 64) * half + c;
-                        tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, dblk);
-                    }
-                }
-                if (lane == 0) bulk_commit_group();
             }
             tc_fence_before();
             mbar_arrive(&sm.dq_free);
         }
         if (lane == 0) bulk_wait_group0();     // every reduce of this warp has landed
         __syncwarp();
-        // dK, dV rows of this tile, d columns of this half
+        (void)ok;
+    } else {
+        // ------------------------------------------------------------ dS warps
+        const int w = warp - kPWarps;
+        const int quarter = w & 3, half = w >> 2;
+        const int t = quarter * 32 + lane;                        // kv row / q row = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t ds_addr = smem_u32(sm.ds[0]);
+        const int col0 = half * 64;                               // this warp's 64 q columns
+        const int kj = k0 + t;
+        const bool loader = half == 0;                            // loads the step's D column t
+        const int my_chunk = D / 64 + half;                       // dQ read-out chunk, if any
+        const bool reads_out = my_chunk < D / 32;
+        bool ok = true;
+        auto col_term = [&](int i) -> float {
+            const int h = g * group + i / nq;
+            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + t;
+            if (qi >= a.total_tokens) return 0.f;
+            return a.delta[static_cast<size_t>(h) * a.total_tokens + qi];
+        };
+        float nxt = loader ? col_term(0) : 0.f;
+        for (int i = 0; i < nsteps; ++i) {
+            const int h = g * group + i / nq;
+            const int q0 = tl.seg_start + (tl.t + i % nq) * kTile;
+            const uint32_t ph = i & 1;
+            if (loader) {
+                sm.delta[i & 1][t] = nxt;
+                mbar_arrive(&sm.cols_d[i & 1]);
+                if (i + 1 < nsteps) nxt = col_term(i + 1);
+            }
+            if (!warp_wait(&sm.cols_d[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            const float *DD = sm.delta[i & 1] + col0;
+            // dS^T = P^T * (dP^T - D); P^T read back from TMEM (bf16), masked entries are 0
+            if (!warp_wait(&sm.dp_full, ph, abort_flag, a.status)) { ok = false; break; }
+            if (!warp_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
+            tc_fence_after();
+            // This warp's slice of the dS buffer held its staged dQ(i-1) chunk: it is
+            // reusable once the TMA engine has read it (dK(i-1) / dQ(i-1), its other
+            // readers, completed before dq_full(i-1)). dP(i) ran meanwhile.
+            if (i > 0 && reads_out) {
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t dp[32], pv[16];
+                tmem_ld32(tmem + lane_off + kB + col0 + c * 32, dp);
+                tmem_ld16(tmem + lane_off + kA + col0 + c * 16, pv);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int col = c * 32 + 2 * e;
+                    const float d0 = bf16_lo(pv[e]) * (__uint_as_float(dp[2 * e]) - DD[col]);
+                    const float d1 = bf16_hi(pv[e]) * (__uint_as_float(dp[2 * e + 1]) - DD[col + 1]);
+                    pk[e] = pack_bf16x2(d0, d1);
+                }
+                // row t, q columns col0 + 32c .. +31: atom `half`, 16-byte chunks 4c .. 4c+3
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4) {
+                    const int chunk = c * 4 + v4;
+                    st_shared_v4(ds_addr + half * kAtom + t * 128 + ((chunk ^ (t & 7)) << 4), pk[4 * v4],
+                                 pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.ds_full);
+
+            // dQ(i) read-out of one [32 rows][32 cols] chunk, staged in this warp's
+            // slice of the dS buffer (free: dK(i) and dQ(i) completed) in the 128-
+            // byte-swizzled layout and added by the TMA engine in the background.
+            // Rows past the segment carry exact zeros.
+            if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
+            tc_fence_after();
+            if (reads_out) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + kB + my_chunk * 32, v);
+                tmem_wait_ld();
+                const uint8_t *stage = sm.ds[0] + (quarter + 4 * half) * 4096;
+                const uint32_t stage_addr = smem_u32(stage);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    st_shared_v4(stage_addr + lane * 128 + ((e ^ (lane & 7)) << 4), v[4 * e], v[4 * e + 1],
+                                 v[4 * e + 2], v[4 * e + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (q0 + quarter * 32 < tl.seg_end)   // skip a chunk of padding rows only
+                        tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, h * (D / 32) + my_chunk);
+                    bulk_commit_group();
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sm.dq_free);
+        }
+        if (lane == 0) bulk_wait_group0();     // every reduce of this warp has landed
+        __syncwarp();
+        // dK, dV rows of this tile, d columns [half * D/2, half * D/2 + D/2)
         if (ok && warp_wait(&sm.fin, 0, abort_flag, a.status)) {
             tc_fence_after();
             const bool live = kj < tl.seg_end;
-            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + g) * D + (D / 2) * half;
+            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + g) * D + half * (D / 2);
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
-                const uint32_t col = (which ? kE : kC) + (D / 2) * half;
+                const uint32_t col = (which ? kE : kC) + half * (D / 2);
                 const float mul = which ? a.scale : 1.f;
                 void *base = which ? a.dk : a.dv;
 #pragma unroll
@@ -523,9 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 17) tmem_dealloc(tmem, kTmemCols);
 }
-
 
 template <int D>
 cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t stream)

@@ -1,7 +1,7 @@
 // Forward attention over packed rows with the per-document causal mask.
 //
-// One CTA computes two consecutive 128-row q tiles (X = A, B) of one segment
-// and one q head: O_X = softmax(S_X) V with S_X = scale * Q_X K^T over the kv
+// A persistent CTA (one per SM) takes work units from a shared counter; a unit
+// is two consecutive 128-row q tiles (X = A, B) of one segment and one q head: O_X = softmax(S_X) V with S_X = scale * Q_X K^T over the kv
 // tiles of the same segment up to X's diagonal (page "Sample Packing: attention
 // problems of long-sequence LLM training", section 5.1 "FlashAttention":
 // tiles above a document's diagonal are never visited, the diagonal tile is
@@ -15,7 +15,9 @@
 //                    r). Reads S_X from TMEM, writes P_X as bf16 back into the
 //                    first 64 columns of S_X's TMEM region, rescales O_X in
 //                    TMEM when needed, final normalisation and stores.
-//   warp 8           TMA producer: Q_A, Q_B once, K / V tiles through a 2-stage ring.
+//   warp 8           TMA producer: takes the next work unit, loads Q_A, Q_B and
+//                    streams the K / V tiles through a 2-stage ring that runs
+//                    on across units.
 //   warp 9           MMA issuer: S_X(j) = Q_X K_j^T (both operands in shared
 //                    memory), O_X += P_X(j) V_j (P from TMEM, V from shared
 //                    memory), interleaved A / B so one tile's softmax overlaps
@@ -41,9 +43,11 @@ struct alignas(1024) FwdSmem {
     uint8_t q[2][D / 64][kAtom];
     uint8_t k[kStages][D / 64][kAtom];
     uint8_t v[kStages][D / 64][kAtom];
-    uint64_t q_full;
+    uint64_t q_full, q_empty;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+    uint64_t unit_full[2], unit_empty[2];
+    int4 unit[2];               // work unit in flight: {head (-1: no more work), seg_start, seg_end, first tile}
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -79,6 +83,21 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         : "memory");
 }
 
+struct UnitShape {
+    int tA, n_kv;
+    bool has_b;
+};
+
+__device__ __forceinline__ UnitShape unit_shape(const int4 &u)
+{
+    UnitShape r;
+    const int n_seg_tiles = (u.z - u.y + kTile - 1) / kTile;
+    r.tA = u.w;
+    r.has_b = r.tA + 1 < n_seg_tiles;
+    r.n_kv = r.has_b ? r.tA + 2 : r.tA + 1;
+    return r;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnFwdArgs a)
 {
@@ -88,21 +107,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (*reinterpret_cast<volatile int *>(a.status) != 0) return;
-    // Head-major order: the CTAs of one head (and the heads of one kv group)
-    // run together, so the K / V tiles they share stay in L2; inside a head the
-    // work list is longest-first.
-    const int h = blockIdx.x / a.grid_tiles;
-    const int unit_idx = blockIdx.x % a.grid_tiles;
-    if (unit_idx >= *a.tile_count) return;
-    const Tile tl = a.tiles[unit_idx];
-    const int n_seg_tiles = (tl.seg_end - tl.seg_start + kTile - 1) / kTile;
-    const int tA = tl.t;                          // q tile of A; B is tA + 1 if the segment has it
-    const bool has_b = tA + 1 < n_seg_tiles;
-    const int n_kv = has_b ? tA + 2 : tA + 1;     // kv tiles the CTA loads
-    const int g = h / (a.Hq / a.Hkv);
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
+        mbar_init(&sm.q_empty, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.k_full[s], 1);
             mbar_init(&sm.v_full[s], 1);
@@ -112,6 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(&sm.s_full[x], 1);
             mbar_init(&sm.p_full[x], 128);
             mbar_init(&sm.o_done[x], 1);
+            mbar_init(&sm.o_free[x], 128);
+            mbar_init(&sm.unit_full[x], 1);
+            mbar_init(&sm.unit_empty[x], 9);   // MMA thread + one lane of each softmax warp
         }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
@@ -132,36 +143,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort_flag = &sm.abort_flag;
     constexpr uint32_t kTileBytes = 128 * D * 2;
-    const int q0A = tl.seg_start + tA * kTile;
+    const int units_per_head = *a.tile_count;
+    const int total_units = units_per_head * a.Hq;
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
+        // Takes work units from the shared counter in list order: head-major
+        // (the CTAs on one head run together, so the K / V tiles they share stay
+        // in L2), longest first inside a head.
         if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.q_full, (has_b ? 2 : 1) * kTileBytes);
-            for (int x = 0; x < (has_b ? 2 : 1); ++x)
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm.q[x][c], &a.tm_q, c * 64, h, q0A + x * kTile, &sm.q_full);
-            int last_use[kStages];
-            for (int s = 0; s < kStages; ++s) last_use[s] = -1;
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j % kStages, u = j / kStages;
-                if (u > 0 && !mbar_wait(&sm.kv_empty[st], (u - 1) & 1, abort_flag, a.status)) break;
-                const int kv0 = tl.seg_start + j * kTile;
-                mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm.k[st][c], &a.tm_k, c * 64, g, kv0, &sm.k_full[st]);
-                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-                for (int c = 0; c < D / 64; ++c)
-                    tma_load_3d(sm.v[st][c], &a.tm_v, c * 64, g, kv0, &sm.v_full[st]);
-                last_use[st] = u;
+            uint32_t kv_iter = 0;
+            int last_kv_use[kStages] = {-1, -1};
+            int q_loads = 0;
+            for (int it = 0;; ++it) {
+                const int slot = it & 1;
+                if (it >= 2 && !mbar_wait(&sm.unit_empty[slot], ((it >> 1) - 1) & 1, abort_flag, a.status)) break;
+                const int u = *abort_flag ? total_units : atomicAdd(a.work_counter, 1);
+                int4 d = make_int4(-1, 0, 0, 0);
+                if (u < total_units) {
+                    const Tile tl = a.tiles[u % units_per_head];
+                    d = make_int4(u / units_per_head, tl.seg_start, tl.seg_end, tl.t);
+                }
+                sm.unit[slot] = d;
+                mbar_arrive(&sm.unit_full[slot]);
+                if (d.x < 0) break;
+                const UnitShape us = unit_shape(d);
+                const int h = d.x, g = h / (a.Hq / a.Hkv);
+                const int q0A = d.y + us.tA * kTile;
+                // Q_A, Q_B once the previous unit's last S MMA has read them
+                if (it > 0 && !mbar_wait(&sm.q_empty, (it - 1) & 1, abort_flag, a.status)) break;
+                mbar_arrive_expect_tx(&sm.q_full, (us.has_b ? 2 : 1) * kTileBytes);
+                for (int x = 0; x < (us.has_b ? 2 : 1); ++x)
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_3d(sm.q[x][c], &a.tm_q, c * 64, h, q0A + x * kTile, &sm.q_full);
+                ++q_loads;
+                bool ok = true;
+                for (int j = 0; j < us.n_kv; ++j, ++kv_iter) {
+                    const int st = kv_iter % kStages, use = kv_iter / kStages;
+                    if (use > 0 && !mbar_wait(&sm.kv_empty[st], (use - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                    const int kv0 = d.y + j * kTile;
+                    mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_3d(sm.k[st][c], &a.tm_k, c * 64, g, kv0, &sm.k_full[st]);
+                    mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                    for (int c = 0; c < D / 64; ++c)
+                        tma_load_3d(sm.v[st][c], &a.tm_v, c * 64, g, kv0, &sm.v_full[st]);
+                    last_kv_use[st] = use;
+                }
+                if (!ok) break;
             }
             if (*abort_flag) {
                 // Let the copies still in flight land before the CTA exits.
-                wait_drain(&sm.q_full, 0);
+                if (q_loads > 0) wait_drain(&sm.q_full, (q_loads - 1) & 1);
                 for (int s = 0; s < kStages; ++s)
-                    if (last_use[s] >= 0) {
-                        wait_drain(&sm.k_full[s], last_use[s] & 1);
-                        wait_drain(&sm.v_full[s], last_use[s] & 1);
+                    if (last_kv_use[s] >= 0) {
+                        wait_drain(&sm.k_full[s], last_kv_use[s] & 1);
+                        wait_drain(&sm.v_full[s], last_kv_use[s] & 1);
                     }
             }
         }
@@ -170,54 +207,87 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
-            const int n_tile0 = tA + 1, n_tile1 = has_b ? tA + 2 : 0;  // kv tiles each q tile reads
-            int empty_commits[kStages] = {};
-            auto issue_s = [&](int x, int j) {
-                const uint32_t q_addr = smem_u32(sm.q[x][0]);
-                const uint32_t k_addr = smem_u32(sm.k[j % kStages][0]);
+            uint32_t kv_iter = 0;
+            int empty_commits[kStages] = {0, 0};
+            int q_commits = 0;
+            uint32_t p_cnt0 = 0, p_cnt1 = 0;      // P tiles consumed, per q tile slot
+            uint32_t o_cnt0 = 0, o_cnt1 = 0;      // units that used O_A / O_B
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int slot = it & 1;
+                if (!mbar_wait(&sm.unit_full[slot], (it >> 1) & 1, abort_flag, a.status)) break;
+                const int4 d = sm.unit[slot];
+                mbar_arrive(&sm.unit_empty[slot]);
+                if (d.x < 0) break;
+                const UnitShape us = unit_shape(d);
+                const int n_tile0 = us.tA + 1, n_tile1 = us.has_b ? us.tA + 2 : 0;  // kv tiles each q tile reads
+                int s_left = n_tile0 + n_tile1;   // S MMAs of this unit still to issue
+                auto issue_s = [&](int x, int j) {
+                    const uint32_t q_addr = smem_u32(sm.q[x][0]);
+                    const uint32_t k_addr = smem_u32(sm.k[(kv_iter + j) % kStages][0]);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    umma_bf16(tmem + x * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                              idesc_s, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&sm.s_full[x]);
-            };
-            auto issue_pv = [&](int x, int j) {
-                const uint32_t v_addr = smem_u32(sm.v[j % kStages][0]);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
+                        umma_bf16(tmem + x * 128, sdesc_sw128(q_addr + off, 16, 1024),
+                                  sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&sm.s_full[x]);
+                    if (--s_left == 0) {             // Q_A / Q_B fully read: next unit may load
+                        umma_commit(&sm.q_empty);
+                        ++q_commits;
+                    }
+                };
+                auto issue_pv = [&](int x, int j) {
+                    const uint32_t v_addr = smem_u32(sm.v[(kv_iter + j) % kStages][0]);
 #pragma unroll
-                for (int kk = 0; kk < 128 / 16; ++kk)
-                    umma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, sdesc_sw128(v_addr + kk * 2048, kAtom, 1024),
-                                 idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            };
-            bool ok = mbar_wait(&sm.q_full, 0, abort_flag, a.status) &&
-                      mbar_wait(&sm.k_full[0], 0, abort_flag, a.status);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0, 0);
-                if (n_tile1 > 0) issue_s(1, 0);
-            }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int st = j % kStages;
-                const bool next_k = j + 1 < n_kv;
-                if (!mbar_wait(&sm.v_full[st], (j / kStages) & 1, abort_flag, a.status)) { ok = false; break; }
-                if (next_k && !mbar_wait(&sm.k_full[(j + 1) % kStages], ((j + 1) / kStages) & 1, abort_flag, a.status)) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int nt = x ? n_tile1 : n_tile0;
-                    if (!ok || j >= nt) continue;
-                    if (!mbar_wait(&sm.p_full[x], j & 1, abort_flag, a.status)) { ok = false; continue; }
-                    tc_fence_after();
-                    issue_pv(x, j);
-                    if (j + 1 < nt) issue_s(x, j + 1);   // its commit also covers this P V
-                    else umma_commit(&sm.o_done[x]);
-                }
+                    for (int kk = 0; kk < 128 / 16; ++kk)
+                        umma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8,
+                                     sdesc_sw128(v_addr + kk * 2048, kAtom, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                };
+                ok = mbar_wait(&sm.q_full, it & 1, abort_flag, a.status) &&
+                     mbar_wait(&sm.k_full[kv_iter % kStages], (kv_iter / kStages) & 1, abort_flag, a.status);
                 if (!ok) break;
-                umma_commit(&sm.kv_empty[st]);
-                ++empty_commits[st];
+                tc_fence_after();
+                issue_s(0, 0);                        // S regions: the last P V of each tile ran before
+                if (n_tile1 > 0) issue_s(1, 0);
+                for (int j = 0; ok && j < us.n_kv; ++j) {
+                    const uint32_t kvj = kv_iter + j;
+                    const int st = kvj % kStages;
+                    const bool next_k = j + 1 < us.n_kv;
+                    if (!mbar_wait(&sm.v_full[st], (kvj / kStages) & 1, abort_flag, a.status)) { ok = false; break; }
+                    if (next_k && !mbar_wait(&sm.k_full[(kvj + 1) % kStages], ((kvj + 1) / kStages) & 1, abort_flag,
+                                             a.status)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const int nt = x ? n_tile1 : n_tile0;
+                        if (!ok || j >= nt) continue;
+                        uint32_t &pc = x ? p_cnt1 : p_cnt0;
+                        if (!mbar_wait(&sm.p_full[x], pc & 1, abort_flag, a.status)) { ok = false; continue; }
+                        ++pc;
+                        if (j == 0) {                 // O_X must have been read out by the last unit's epilogue
+                            const uint32_t oc = x ? o_cnt1 : o_cnt0;
+                            if (oc > 0 && !mbar_wait(&sm.o_free[x], (oc - 1) & 1, abort_flag, a.status)) {
+                                ok = false;
+                                continue;
+                            }
+                        }
+                        tc_fence_after();
+                        issue_pv(x, j);
+                        if (j + 1 < nt) issue_s(x, j + 1);   // its commit also covers this P V
+                        else {
+                            umma_commit(&sm.o_done[x]);
+                            if (x) ++o_cnt1;
+                            else ++o_cnt0;
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&sm.kv_empty[st]);
+                    ++empty_commits[st];
+                }
+                kv_iter += us.n_kv;
             }
             // Every arrive the tensor core owes this CTA's barriers must land
             // before the CTA exits.
@@ -225,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             wait_drain(&sm.drain, 0);
             for (int s = 0; s < kStages; ++s)
                 if (empty_commits[s] > 0) wait_drain(&sm.kv_empty[s], (empty_commits[s] - 1) & 1);
+            if (q_commits > 0) wait_drain(&sm.q_empty, (q_commits - 1) & 1);
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -232,90 +303,102 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int r = threadIdx.x & 127;              // q row within the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t s_col = x * 128, o_col = 256 + x * 128;
-        const int tX = tA + x;
-        const int nX = (x == 0) ? tA + 1 : (has_b ? tA + 2 : 0);
         const float sl2 = a.scale_log2;
-        float m = -INFINITY, l = 0.f;
+        uint32_t s_cnt = 0, o_cnt = 0;                // S tiles and units this warpgroup consumed
         bool ok = true;
-        for (int j = 0; j < nX; ++j) {
-            if (!warp_wait(&sm.s_full[x], j & 1, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            const bool diag = (j == tX);
-            // pass 1: row max, 64 columns per TMEM round trip, 8 independent chains
-            float mxs[8];
+        for (int it = 0; ok; ++it) {
+            const int slot = it & 1;
+            if (!warp_wait(&sm.unit_full[slot], (it >> 1) & 1, abort_flag, a.status)) break;
+            const int4 d = sm.unit[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);
+            if (d.x < 0) break;
+            const UnitShape us = unit_shape(d);
+            if (x == 1 && !us.has_b) continue;
+            const int h = d.x;
+            const int tX = us.tA + x;
+            const int nX = tX + 1;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < nX; ++j) {
+                if (!warp_wait(&sm.s_full[x], s_cnt & 1, abort_flag, a.status)) { ok = false; break; }
+                ++s_cnt;
+                tc_fence_after();
+                const bool diag = (j == tX);
+                // pass 1: row max, 64 columns per TMEM round trip, 8 independent chains
+                float mxs[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) mxs[e] = -INFINITY;
+                for (int e = 0; e < 8; ++e) mxs[e] = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t sv[64];
-                tmem_ld32(tmem + lane_off + s_col + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tmem_ld32(tmem + lane_off + s_col + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                tmem_wait_ld();
-                if (diag) {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e)
-                        if (c * 64 + e <= r) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
-                }
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                   fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
-            const float m_new = fmaxf(m, mx * sl2);
-            const bool need = m_new > m + 8.0f;
-            if (__any_sync(0xffffffffu, need)) {
-                const float m_use = need ? m_new : m;
-                const float alpha = ex2(m - m_use);  // 0 when m = -inf
-                if (j > 0) {
-                    // O_X is stable: the commit that raised s_full covers the last P V.
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_off + o_col + c * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tmem + lane_off + o_col + c * 32, o);
-                    }
-                }
-                l *= alpha;
-                m = m_use;
-            }
-            // pass 2: P = 2^(S * scale * log2 e - m), written as bf16 over the
-            // first 64 columns of S_X's region; P columns 32c..32c+31 only cover
-            // S columns already read.
-            float sums[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t sv[64];
-                tmem_ld32(tmem + lane_off + s_col + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                tmem_ld32(tmem + lane_off + s_col + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                tmem_wait_ld();
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - m);
-                    float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - m);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t sv[64];
+                    tmem_ld32(tmem + lane_off + s_col + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                    tmem_ld32(tmem + lane_off + s_col + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                    tmem_wait_ld();
                     if (diag) {
-                        if (c * 64 + 2 * e > r) p0 = 0.f;
-                        if (c * 64 + 2 * e + 1 > r) p1 = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 64; ++e)
+                            if (c * 64 + e <= r) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 64; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
                     }
-                    sums[e & 3] += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
                 }
-                tmem_st32(tmem + lane_off + s_col + c * 32, pk);
+                const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
+                                       fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+                const float m_new = fmaxf(m, mx * sl2);
+                const bool need = m_new > m + 8.0f;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_use = need ? m_new : m;
+                    const float alpha = ex2(m - m_use);  // 0 when m = -inf
+                    if (j > 0) {
+                        // O_X is stable: the commit that raised s_full covers the last P V.
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tmem + lane_off + o_col + c * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                            tmem_st32(tmem + lane_off + o_col + c * 32, o);
+                        }
+                    }
+                    l *= alpha;
+                    m = m_use;
+                }
+                // pass 2: P = 2^(S * scale * log2 e - m), written as bf16 over the
+                // first 64 columns of S_X's region; P columns 32c..32c+31 only cover
+                // S columns already read.
+                float sums[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t sv[32];
+                    tmem_ld32(tmem + lane_off + s_col + c * 32, sv);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - m);
+                        float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - m);
+                        if (diag) {
+                            if (c * 32 + 2 * e > r) p0 = 0.f;
+                            if (c * 32 + 2 * e + 1 > r) p1 = 0.f;
+                        }
+                        sums[e & 3] += p0 + p1;
+                        pk[e] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tmem + lane_off + s_col + c * 16, pk);
+                }
+                l += (sums[0] + sums[1]) + (sums[2] + sums[3]);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.p_full[x]);
             }
-            const float sum = (sums[0] + sums[1]) + (sums[2] + sums[3]);
-            l += sum;
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&sm.p_full[x]);
-        }
-        if (ok && nX > 0 && warp_wait(&sm.o_done[x], 0, abort_flag, a.status)) {
+            if (!ok) break;
+            // epilogue: normalise O_X and store it with the row's LSE
+            if (!warp_wait(&sm.o_done[x], o_cnt & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
-            const int qi = q0A + x * kTile + r;
-            const bool valid = qi < tl.seg_end;
+            const int qi = d.y + tX * kTile + r;
+            const bool valid = qi < d.z;
             const float inv_l = 1.f / l;
             uint16_t *orow = a.out + (static_cast<size_t>(qi) * a.Hq + h) * D;
 #pragma unroll
@@ -334,6 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 }
             }
             if (valid) a.lse[static_cast<size_t>(h) * a.total_tokens + qi] = (m + log2f(l)) * 0.69314718055994531f;
+            tc_fence_before();
+            mbar_arrive(&sm.o_free[x]);
+            ++o_cnt;
         }
     }
 
@@ -353,13 +439,15 @@ cudaError_t launch_fwd_d(const AttnFwdArgs &a, int64_t grid_units, cudaStream_t 
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    AttnFwdArgs a2 = a;
-    a2.grid_tiles = static_cast<int32_t>(grid_units);
-    const int64_t grid = grid_units * a.Hq;
+    // Persistent: one CTA per SM takes work units from the shared counter.
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int64_t grid = grid_units * a.Hq;
+    if (grid > sms) grid = sms;
     if (grid <= 0) return cudaSuccess;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
     prof_begin(kProfAttnFwd, stream);
-    attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a2);
+    attn_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
     prof_end(kProfAttnFwd, stream);
     return cudaGetLastError();
 }

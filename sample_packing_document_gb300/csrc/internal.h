@@ -100,6 +100,7 @@ struct AttnFwdArgs {
     float *lse;
     const Tile *tiles;
     const int32_t *tile_count;
+    int32_t *work_counter;  // next work unit (zeroed by the scheduler kernel)
     int *status;
     int32_t total_tokens;
     int32_t Hq, Hkv;

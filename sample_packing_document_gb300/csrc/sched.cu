@@ -21,7 +21,7 @@ namespace spd {
 namespace {
 
 constexpr int kThreads = 1024;
-constexpr int kCostCap = 4095;  // costs above this share one bin (order among them is free)
+constexpr int kCostCap = 4 * kThreads - 1;  // costs above this share one bin (order among them is free)
 
 __device__ long long block_scan_excl(long long v, long long *total, long long *sh)
 {
@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
     const int tid = threadIdx.x;
     if (tid == 0) {
         *status = 0;
+        count[1] = 0;   // work counter of the persistent kernels
         bad_s = 0;
     }
     for (int c = tid; c <= kCostCap; c += kThreads) bins[c] = 0;
@@ -115,12 +116,20 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
     }
     __syncthreads();
     // Descending exclusive scan: bins[c] <- number of tiles with a larger cost.
-    if (tid == 0) {
-        int run = 0;
-        for (int c = kCostCap; c >= 0; --c) {
-            int v = bins[c];
-            bins[c] = run;
-            run += v;
+    // Thread tid owns costs kCostCap - 4 tid .. kCostCap - 4 tid - 3.
+    {
+        int v[4], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            v[k] = bins[kCostCap - (4 * tid + k)];
+            sum += v[k];
+        }
+        long long tot;
+        long long run = block_scan_excl(sum, &tot, sh);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            bins[kCostCap - (4 * tid + k)] = static_cast<int>(run);
+            run += v[k];
         }
     }
     __syncthreads();
