@@ -82,8 +82,9 @@ def flops(seg_lens, Hq, d):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms; summary()
+    keeps the samples taken inside a host-time window."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -111,22 +112,27 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self):
+    def summary(self, t0, t1):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        import datetime
         mhz, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
             for line in open(self.path):
                 f = [x.strip() for x in line.split(",")]
-                if len(f) < 9:
+                if len(f) < 10:
                     continue
                 try:
-                    mhz.append(float(f[1]))
-                    mx = float(f[2])
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    sm, smax = float(f[2]), float(f[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, f[5:9]):
+                if not (t0 <= ts <= t1):
+                    continue
+                mhz.append(sm)
+                mx = smax
+                for n, v in zip(names, f[6:10]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
         finally:
@@ -351,9 +357,10 @@ def main():
             e.record(stream)    # creates the CUDA event; the library re-records it around its kernel
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
-        time.sleep(0.3)
+        time.sleep(0.5)                      # nvidia-smi has started sampling
         dist_barrier(ws_n)
         torch.cuda.synchronize()
+        host_t0 = time.time()
         t_start.record(stream)
         for i in range(args.steps):
             ops.pack_tokens(toks_d, lens_d, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk)
@@ -364,8 +371,19 @@ def main():
             ops.set_profile_events(None, None, ops.PROFILE_NONE)
         t_end.record(stream)
         torch.cuda.synchronize()
+        host_t1 = time.time()
         dist_barrier(ws_n)
-    clocks = clk.summary()
+        extra = 0
+        if host_t1 - host_t0 < 2.0:
+            # A short timed region holds few 200 ms samples: keep running the
+            # same step (untimed) so the clock record covers at least 2 s.
+            while time.time() - host_t0 < 2.0:
+                step()
+                torch.cuda.synchronize()
+                extra += 1
+        host_t2 = time.time()
+    clocks = clk.summary(host_t0, host_t2)
+    clocks["window"] = "timed region" + (" + %d identical untimed steps" % extra if extra else "")
     ms_local = t_start.elapsed_time(t_end) / args.steps
     ms = dist_max(ms_local, ws_n)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["fwd"])
