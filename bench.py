@@ -339,7 +339,9 @@ def main():
         ops.varlen_attn_fwd(q, k, v, cu, ns, out=out, lse=lse, ws=ws_f)
         ops.varlen_attn_bwd(q, k, v, out, do, lse, cu, ns, dq=dq, dk=dk, dv=dv, ws=ws_b)
 
-    launches_per_step = 2 + 2 + 4   # pack: scan + stream; fwd: schedule + main; bwd: schedule + pre + main + dq
+    # pack: one fused launch (few documents) or scan + stream; fwd: schedule + main;
+    # bwd: schedule + pre + main + dq
+    launches_per_step = (1 if (w.use_packed_dataset and len(lens) <= 1024) else 2) + 2 + 4
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize()
@@ -400,6 +402,8 @@ def main():
                 "flops_per_launch": fl["bwd"], "ms_per_launch": bwd_ms}
     fwd_tf = fl["fwd"] / (fwd_ms * 1e-3) / 1e12
 
+    pack = pack_measure(ops, dev) if rank == 0 else None
+
     e2e = None
     if not args.no_e2e:
         e2e = e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev)
@@ -418,13 +422,52 @@ def main():
                 "flops_per_step": fl["total"], "strict_flops_value": ws_n * fl["strict_total"] / (ms * 1e-3) / 1e12,
                 "kernels_ms": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms},
                 "kernels_tflops": {"attn_fwd": fwd_tf, "attn_bwd": bwd_tf},
-                "roofline": roofline, "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+                "roofline": roofline, "pack_tokens": pack, "clocks": clocks, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps,
                 "cpu_baseline": cpu}
         print(json.dumps(line))
     if ws_n > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def pack_measure(ops, dev, name="c5", reps=20):
+    """spd_pack_tokens alone on a workload's documents (device-resident),
+    L2 flushed between repetitions; algorithmic bytes / time."""
+    import torch
+    w, lens, toks = workload_docs(name)
+    toks_d, lens_d = torch.tensor(toks, device=dev), torch.tensor(lens, device=dev)
+    out = ops.alloc_pack_outputs(len(lens), len(toks), w.micro_bsz, w.seq_len, w.use_packed_dataset, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    segs = len(segment_lengths(lens, w))
+    npos = out["rows"] * w.micro_bsz * w.seq_len
+    nbytes = 4 * len(toks) + 4 * len(lens) + 12 * npos + 4 * (segs + 1) + 4 * (2 * out["rows"] + 2)
+    times = []
+    fused = w.use_packed_dataset and len(lens) <= 1024
+    for it in range(reps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        b.record()
+        # events recorded by the library right around the kernel launch, so the
+        # host's call overhead is not timed (one fused launch for this case)
+        ops.set_profile_events(a, b, ops.PROFILE_PACK_STREAM)
+        ops.pack_tokens(toks_d, lens_d, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=out)
+        ops.set_profile_events(None, None, ops.PROFILE_NONE)
+        torch.cuda.synchronize()
+        if it >= 3:
+            times.append(a.elapsed_time(b))
+    if ops.read_status(out["ws"]) != 0:
+        raise RuntimeError("pack status")
+    ms = statistics.median(times)
+    pk, how = peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "%s documents: %d tokens, %d documents, one row of %d" % (name, len(toks), len(lens), npos),
+            "ms": ms, "bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / pk.get("hbm_gbs", 6800.0),
+            "frac_8TBs": gbs / 8000.0,
+            "timing": ("%s, CUDA events around the launch, L2 flushed, median of %d" %
+                       ("the whole call (one fused kernel)" if fused else "the token-stream kernel only", reps))}
 
 
 def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):

@@ -8,7 +8,8 @@
 // (cu_seqlens: segment boundaries of a row, the padding tail being its own
 // segment; indexes: position inside the current segment).
 //
-// Two launches on one stream:
+// build_pack with at most 1024 documents and 512 rows runs as one fused
+// launch (pack_fused_kernel). Otherwise, two launches on one stream:
 //   pack_scan_kernel    one CTA: prefix sums over the document lengths, the
 //                       document -> output position map, cu_seqlens,
 //                       row_seg_ptr, max_seqlen, num_segs. Work ~ num_docs.
@@ -325,6 +326,215 @@ __global__ void __launch_bounds__(kStreamThreads) pack_stream_kernel(PackArgs a)
     }
 }
 
+// ---------------------------------------------------------------- fused path
+// build_pack with few documents and rows (the common case): one launch. Every
+// CTA scans the document lengths itself into shared memory (they are a few KB
+// and stay in L2); CTA 0 then writes the segment fields and the status word,
+// every other CTA 1024 output positions. Same rules and outputs as the
+// two-kernel path.
+constexpr int kFusedThreads = 256;
+constexpr int kFusedDocs = 1024;   // documents the fused path accepts
+constexpr int kFusedRows = 512;    // rows the fused path accepts
+constexpr int kFusedIters = 1;
+constexpr int kFusedChunk = kFusedThreads * 4 * kFusedIters;
+
+__device__ int block_excl_scan256(int v, int *total, int *sh)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kFusedThreads / 32 ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kFusedThreads / 32) sh[lane] = w;
+    }
+    __syncthreads();
+    const int r = (warp ? sh[warp - 1] : 0) + x - v;
+    *total = sh[kFusedThreads / 32 - 1];
+    __syncthreads();
+    return r;
+}
+
+// Largest d in [0, n) with a[d] <= x; assumes a[0] <= x.
+__device__ __forceinline__ int last_le_smem(const int32_t *a, int n, long long x)
+{
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (a[mid] <= x) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(kFusedThreads) pack_fused_kernel(PackArgs a)
+{
+    __shared__ int32_t s_start[kFusedDocs + 1];
+    __shared__ int sh[32];
+    __shared__ int bad_s;
+    const int tid = threadIdx.x;
+    const int nd = a.num_docs;
+    // all positions fit in int32 (rows * plen <= 2^31 - 1 is checked on the host)
+    const int plen = a.plen, total = a.num_tokens;
+    const int npos = a.rows * plen;
+    if (tid == 0) bad_s = 0;
+
+    // The token loads need no document boundaries: issue them first so their
+    // latency overlaps the scan. tk[k] = tokens[p + k], k = 0..4 (k = 4 feeds
+    // the label of position p + 3).
+    const int p = static_cast<int>(blockIdx.x - 1) * kFusedChunk + tid * 4;
+    int32_t tk[5];
+#pragma unroll
+    for (int k = 0; k < 5; ++k)
+        tk[k] = (blockIdx.x > 0 && p + k < total) ? __ldg(a.tokens + p + k) : 0;
+
+    // document starts: exclusive scan of the lengths, 4 per thread
+    {
+        int len[4];
+        long long sum64 = 0;
+        bool bad = false;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = tid * 4 + k;
+            len[k] = d < nd ? a.doc_lens[d] : 0;
+            if (d < nd && len[k] <= 0) bad = true;
+            if (len[k] < 0) len[k] = 0;
+            sum64 += len[k];
+        }
+        // valid lengths sum to num_tokens <= 2^31 - 1, so any partial sum above it is bad
+        if (sum64 > a.num_tokens) bad = true;
+        const int sum = bad ? 0 : static_cast<int>(sum64);
+        if (bad) atomicOr(&bad_s, 1);
+        int tot;
+        int e = block_excl_scan256(sum, &tot, sh);
+        long long run = e;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = tid * 4 + k;
+            if (d < nd) s_start[d] = static_cast<int32_t>(run);
+            run += len[k];
+        }
+        if (tid == 0) {
+            s_start[nd] = tot;
+            if (tot != a.num_tokens) bad_s = 1;
+        }
+    }
+    __syncthreads();
+    if (bad_s) {
+        if (blockIdx.x == 0 && tid == 0) {
+            *a.status = kErrBadDocs;   // CTA 0 alone owns the status word in this launch
+            *a.num_segs = 0;
+        }
+        return;
+    }
+
+    // CTA 0 writes the segment fields; CTAs 1.. write 1024 output positions each,
+    // four consecutive positions per thread
+    if (blockIdx.x > 0 && p < npos) {
+        int32_t id[4], lab[4], idx[4];
+        int d = p < total ? last_le_smem(s_start, nd, p) : 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q = p + k;
+            if (q >= npos) { id[k] = lab[k] = idx[k] = 0; continue; }
+            if (q >= total) {
+                id[k] = 0;
+                lab[k] = -100;
+                idx[k] = q - total;
+                continue;
+            }
+            while (d + 1 < nd && s_start[d + 1] <= q) ++d;
+            const int start = s_start[d], end = s_start[d + 1];
+            id[k] = tk[k];
+            lab[k] = (q + 1 < end) ? tk[k + 1] : -100;
+            const int row_start = (q / plen) * plen;
+            idx[k] = q - (start > row_start ? start : row_start);
+        }
+        if (a.vec_out && p + 4 <= npos) {
+            *reinterpret_cast<int4 *>(a.input_ids + p) = make_int4(id[0], id[1], id[2], id[3]);
+            *reinterpret_cast<int4 *>(a.labels + p) = make_int4(lab[0], lab[1], lab[2], lab[3]);
+            *reinterpret_cast<int4 *>(a.indexes + p) = make_int4(idx[0], idx[1], idx[2], idx[3]);
+        } else {
+            for (int k = 0; k < 4 && p + k < npos; ++k) {
+                a.input_ids[p + k] = id[k];
+                a.labels[p + k] = lab[k];
+                a.indexes[p + k] = idx[k];
+            }
+        }
+    }
+    if (blockIdx.x != 0) return;
+
+    // CTA 0: segment boundaries are the union of document starts, row starts and
+    // the padding start; a document start on a row start is the same boundary
+    // (counted by the "aligned" scan so ranks stay exact).
+    __shared__ int32_t s_aligned[kFusedDocs + 1];   // aligned starts before document d
+    __shared__ int32_t s_cu[kFusedDocs + 2 * kFusedRows + 1];
+    __shared__ int32_t s_max[kFusedRows];
+    {
+        int f[4], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = tid * 4 + k;
+            f[k] = (d >= 1 && d < nd && (s_start[d] % plen) == 0) ? 1 : 0;
+            sum += f[k];
+        }
+        int tot;
+        int run = block_excl_scan256(sum, &tot, sh);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = tid * 4 + k;
+            if (d <= nd) s_aligned[d] = run;
+            run += f[k];
+        }
+        if (tid == 0) s_aligned[nd] = tot;
+    }
+    for (int r = tid; r < a.rows; r += kFusedThreads) s_max[r] = 0;
+    __syncthreads();
+    const int pad = (total % plen) != 0;
+    const int num_segs = a.rows == 0 ? 0 : static_cast<int>(a.rows + nd - 1 - s_aligned[nd] + pad);
+    for (int d = tid; d < nd; d += kFusedThreads) {
+        const int st = s_start[d];
+        if (d >= 1 && (st % plen) != 0) s_cu[(st - 1) / plen + d - s_aligned[d]] = st;
+    }
+    for (int r = tid; r <= a.rows; r += kFusedThreads) {
+        int rank = 0;
+        if (r > 0) {
+            // first document starting at or after r * plen
+            const int x = r * plen;
+            int lo = 0, hi = nd;
+            while (lo < hi) {
+                int mid = (lo + hi) >> 1;
+                if (s_start[mid] < x) lo = mid + 1;
+                else hi = mid;
+            }
+            rank = r + lo - 1 - s_aligned[lo] + ((r == a.rows && pad) ? 1 : 0);
+        }
+        s_cu[rank] = r * plen;
+        a.row_seg_ptr[r] = rank;
+    }
+    if (tid == 0 && pad) s_cu[num_segs - 1] = total;
+    __syncthreads();
+    for (int i = tid; i <= num_segs; i += kFusedThreads) a.cu_seqlens[i] = s_cu[i];
+    for (int i = tid; i < num_segs; i += kFusedThreads)
+        atomicMax(&s_max[s_cu[i] / plen], s_cu[i + 1] - s_cu[i]);
+    __syncthreads();
+    for (int r = tid; r < a.rows; r += kFusedThreads) a.max_seqlen[r] = s_max[r];
+    if (tid == 0) {
+        *a.num_segs = num_segs;
+        *a.status = 0;
+    }
+}
+
 }  // namespace
 
 size_t pack_ws_bytes(int64_t num_docs)
@@ -344,11 +554,17 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
     a.doc_keep = reinterpret_cast<int32_t *>(ws + kWsHeader + 2 * arr);
     int32_t *aux = reinterpret_cast<int32_t *>(ws + kWsHeader + 3 * arr);
 
+    const long long npos = static_cast<long long>(a.rows) * a.plen;
+    if (a.packed && a.num_docs >= 1 && a.num_docs <= kFusedDocs && a.rows <= kFusedRows) {
+        prof_begin(kProfPackStream, stream);
+        pack_fused_kernel<<<static_cast<unsigned>(1 + (npos + kFusedChunk - 1) / kFusedChunk), kFusedThreads, 0,
+                            stream>>>(a);
+        prof_end(kProfPackStream, stream);
+        return cudaGetLastError();
+    }
     pack_scan_kernel<<<1, kScanThreads, 0, stream>>>(a, aux);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-
-    const long long npos = static_cast<long long>(a.rows) * a.plen;
     if (npos == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((npos + kChunk - 1) / kChunk));
