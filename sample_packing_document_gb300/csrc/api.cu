@@ -337,6 +337,7 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.grad_fp32 = grad_dtype;
     a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
     a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
+    a.work_counter = reinterpret_cast<int32_t *>(base) + 2;
     a.status = reinterpret_cast<int *>(base);
     a.total_tokens = static_cast<int32_t>(total_tokens);
     a.Hq = Hq;

@@ -39,6 +39,8 @@
 #include "internal.h"
 #include "ptx.cuh"
 
+#include <type_traits>
+
 namespace spd {
 namespace {
 
@@ -57,11 +59,13 @@ struct BwdSmem {
     uint8_t ds[2][kAtom];            // dS^T: [128 kv rows][128 q cols]
     float lse2[2][128];              // LSE * log2(e) of the step's q columns
     float delta[2][128];             // D of the step's q columns
-    uint64_t kv_full;
+    uint64_t kv_full, kv_empty;
     uint64_t q_full[kQStages], q_empty[kQStages], do_full[kQStages], do_empty[kQStages];
     uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free;
     uint64_t cols_l[2], cols_d[2];   // the step's lse2 / delta written
-    uint64_t fin, drain;
+    uint64_t unit_full[2], unit_empty[2];
+    int4 unit[2];                    // work unit in flight: {kv head (-1: no more work), seg_start, seg_end, kv tile}
+    uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -177,6 +181,8 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
 }
 
 // ------------------------------------------------------------------ main kernel
+__device__ __forceinline__ int seg_tiles(const int4 &u) { return (u.z - u.y + kTile - 1) / kTile; }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ AttnBwdArgs a)
 {
@@ -189,20 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         if (threadIdx.x == 0) set_status(a.status, kErrTimeout);
         return;
     }
-    // kv-head-major order: the CTAs of one kv head run together, so the Q / dO
-    // tiles they share and the dQ rows they add into stay in L2.
-    const int g = blockIdx.x / a.grid_tiles;
-    const int tile_idx = blockIdx.x % a.grid_tiles;
-    if (tile_idx >= *a.tile_count) return;
-    const Tile tl = a.tiles[tile_idx];
     const int group = a.Hq / a.Hkv;
-    const int n_seg_tiles = (tl.seg_end - tl.seg_start + kTile - 1) / kTile;
-    const int nq = n_seg_tiles - tl.t;   // q tiles t .. n-1
-    const int nsteps = group * nq;
-    const int k0 = tl.seg_start + tl.t * kTile;
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.kv_full, 1);
+        mbar_init(&sm.kv_empty, 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&sm.q_full[s], 1);
             mbar_init(&sm.q_empty[s], 4 * (D / 64));  // the P warps that stage dQ there, once it is read
@@ -218,8 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.cols_l[b], 128);
             mbar_init(&sm.cols_d[b], 128);
+            mbar_init(&sm.unit_full[b], 1);
+            mbar_init(&sm.unit_empty[b], 1 + kPWarps + kDsWarps);  // MMA thread + one lane per compute warp
         }
-        mbar_init(&sm.fin, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -233,6 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tma_prefetch_desc(&a.tm_k);
         tma_prefetch_desc(&a.tm_v);
         tma_prefetch_desc(&a.tm_do);
+        tma_prefetch_desc(&a.tm_dqacc);
     }
     tc_fence_before();
     __syncthreads();
@@ -242,33 +241,80 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     constexpr uint32_t kTileBytes = 128 * D * 2;
     constexpr uint32_t kA = 0, kB = 128, kC = 256, kE = 256 + D;
 
+    // Work unit `it` from the two-slot ring, for a whole compute warp.
+    auto warp_unit = [&](int it, int4 &d) -> bool {
+        const int slot = it & 1;
+        if (!warp_wait(&sm.unit_full[slot], (it >> 1) & 1, abort_flag, a.status)) return false;
+        d = sm.unit[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);
+        return true;
+    };
+
     if (warp == 16) {
         // ------------------------------------------------------------ producer
+        // Takes work units (kv head, kv tile) from the shared counter in list
+        // order: kv-head-major, so the CTAs of one kv head run together and the
+        // Q / dO tiles they share and the dQ rows they add into stay in L2;
+        // longest first inside a head. Q / dO stream through a 2-stage ring that
+        // runs on across units; the next unit's K / V are pulled into L2 as soon
+        // as it is taken and copied in once the last MMA reading K has completed.
         if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
-            for (int c = 0; c < D / 64; ++c) {
-                tma_load_3d(sm.k[c], &a.tm_k, c * 64, g, k0, &sm.kv_full);
-                tma_load_3d(sm.v[c], &a.tm_v, c * 64, g, k0, &sm.kv_full);
-            }
+            const int n_tiles = *a.tile_count;
+            const int total_units = n_tiles * a.Hkv;
+            int gi = 0, kv_loads = 0;
             int last_q[kQStages], last_do[kQStages];
             for (int s = 0; s < kQStages; ++s) last_q[s] = last_do[s] = -1;
-            for (int i = 0; i < nsteps; ++i) {
-                const int st = i % kQStages, u = i / kQStages;
-                const int h = g * group + i / nq;
-                const int q0 = tl.seg_start + (tl.t + i % nq) * kTile;
-                if (u > 0 && !mbar_wait(&sm.q_empty[st], (u - 1) & 1, abort_flag, a.status)) break;
+            auto load_step = [&](const int4 &d, int nq, int i, int gs) -> bool {
+                const int st = gs % kQStages, u = gs / kQStages;
+                const int h = d.x * group + i / nq;
+                const int q0 = d.y + (d.w + i % nq) * kTile;
+                if (u > 0 && !mbar_wait(&sm.q_empty[st], (u - 1) & 1, abort_flag, a.status)) return false;
                 mbar_arrive_expect_tx(&sm.q_full[st], kTileBytes);
                 for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q[st][c], &a.tm_q, c * 64, h, q0, &sm.q_full[st]);
                 last_q[st] = u;
-                if (u > 0 && !mbar_wait(&sm.do_empty[st], (u - 1) & 1, abort_flag, a.status)) break;
+                if (u > 0 && !mbar_wait(&sm.do_empty[st], (u - 1) & 1, abort_flag, a.status)) return false;
                 mbar_arrive_expect_tx(&sm.do_full[st], kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_3d(sm.dout[st][c], &a.tm_do, c * 64, h, q0, &sm.do_full[st]);
                 last_do[st] = u;
+                return true;
+            };
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int slot = it & 1;
+                if (it >= 2 && !mbar_wait(&sm.unit_empty[slot], ((it >> 1) - 1) & 1, abort_flag, a.status)) break;
+                const int w = *abort_flag ? total_units : atomicAdd(a.work_counter, 1);
+                int4 d = make_int4(-1, 0, 0, 0);
+                if (w < total_units) {
+                    const Tile tl = a.tiles[w % n_tiles];
+                    d = make_int4(w / n_tiles, tl.seg_start, tl.seg_end, tl.t);
+                }
+                sm.unit[slot] = d;
+                mbar_arrive(&sm.unit_full[slot]);
+                if (d.x < 0) break;
+                const int k0 = d.y + d.w * kTile;
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_prefetch_l2_3d(&a.tm_k, c * 64, d.x, k0);
+                    tma_prefetch_l2_3d(&a.tm_v, c * 64, d.x, k0);
+                }
+                const int nq = seg_tiles(d) - d.w;
+                const int nsteps = group * nq;
+                if (!load_step(d, nq, 0, gi)) break;
+                if (it > 0 && !mbar_wait(&sm.kv_empty, (it - 1) & 1, abort_flag, a.status)) break;
+                mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
+                for (int c = 0; c < D / 64; ++c) {
+                    tma_load_3d(sm.k[c], &a.tm_k, c * 64, d.x, k0, &sm.kv_full);
+                    tma_load_3d(sm.v[c], &a.tm_v, c * 64, d.x, k0, &sm.kv_full);
+                }
+                ++kv_loads;
+                for (int i = 1; i < nsteps; ++i)
+                    if (!load_step(d, nq, i, gi + i)) { ok = false; break; }
+                gi += nsteps;
             }
             if (*abort_flag) {
                 // Let the copies still in flight land before the CTA exits.
-                wait_drain(&sm.kv_full, 0);
+                if (kv_loads > 0) wait_drain(&sm.kv_full, (kv_loads - 1) & 1);
                 for (int s = 0; s < kQStages; ++s) {
                     if (last_q[s] >= 0) wait_drain(&sm.q_full[s], last_q[s] & 1);
                     if (last_do[s] >= 0) wait_drain(&sm.do_full[s], last_do[s] & 1);
@@ -284,9 +330,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             const uint32_t k_addr = smem_u32(sm.k[0]), v_addr = smem_u32(sm.v[0]);
             const uint32_t ds_addr = smem_u32(sm.ds[0]);
             int do_commits[kQStages] = {};
-            auto issue_s = [&](int i) -> bool {   // S^T(i) = K Q(i)^T into A
-                const int st = i % kQStages;
-                if (!mbar_wait(&sm.q_full[st], (i / kQStages) & 1, abort_flag, a.status)) return false;
+            int kv_commits = 0;
+            auto issue_s = [&](int gs) -> bool {   // S^T = K Q^T into A
+                const int st = gs % kQStages;
+                if (!mbar_wait(&sm.q_full[st], (gs / kQStages) & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
                 const uint32_t q_addr = smem_u32(sm.q[st][0]);
 #pragma unroll
@@ -298,10 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 umma_commit(&sm.s_full);
                 return true;
             };
-            auto issue_dp = [&](int i) -> bool {  // dP^T(i) = V dO(i)^T into B, once dQ(i-1) left B
-                const int st = i % kQStages;
-                if (!mbar_wait(&sm.do_full[st], (i / kQStages) & 1, abort_flag, a.status)) return false;
-                if (i > 0 && !mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, a.status)) return false;
+            auto issue_dp = [&](int gs) -> bool {  // dP^T = V dO^T into B, once the previous dQ left B
+                const int st = gs % kQStages;
+                if (!mbar_wait(&sm.do_full[st], (gs / kQStages) & 1, abort_flag, a.status)) return false;
+                if (gs > 0 && !mbar_wait(&sm.dq_free, (gs - 1) & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
                 const uint32_t do_addr = smem_u32(sm.dout[st][0]);
 #pragma unroll
@@ -313,276 +360,269 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 umma_commit(&sm.dp_full);
                 return true;
             };
-            bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, a.status) && issue_s(0) && issue_dp(0);
-            for (int i = 0; ok && i < nsteps; ++i) {
-                const int st = i % kQStages;
-                const uint32_t ph = i & 1;
-                // dV += P^T(i) dO(i): P^T in TMEM over S^T (M = kv, K = q), dO MN-major
-                if (!mbar_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
-                tc_fence_after();
-                {
-                    const uint32_t do_addr = smem_u32(sm.dout[st][0]);
+            bool ok = true;
+            int gi = 0;
+            for (int it = 0; ok; ++it) {
+                const int slot = it & 1;
+                if (!mbar_wait(&sm.unit_full[slot], (it >> 1) & 1, abort_flag, a.status)) break;
+                const int4 d = sm.unit[slot];
+                mbar_arrive(&sm.unit_empty[slot]);
+                if (d.x < 0) break;
+                const int nsteps = group * (seg_tiles(d) - d.w);
+                ok = mbar_wait(&sm.kv_full, it & 1, abort_flag, a.status) && issue_s(gi) && issue_dp(gi);
+                for (int i = 0; ok && i < nsteps; ++i, ++gi) {
+                    const int st = gi % kQStages;
+                    const uint32_t ph = gi & 1;
+                    // dV += P^T dO: P^T in TMEM over S^T (M = kv, K = q), dO MN-major.
+                    // The first step of a unit overwrites the dV the P warps have read out.
+                    if (!mbar_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    {
+                        const uint32_t do_addr = smem_u32(sm.dout[st][0]);
 #pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk)
-                        // P^T q columns 16kk .. 16kk+15 sit at TMEM column 64 (kk / 4) + 8 (kk % 4)
-                        umma_bf16_ts(tmem + kC, tmem + kA + (kk >> 2) * 64 + (kk & 3) * 8,
-                                     sdesc_sw128(do_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 128 / 16; ++kk)
+                            // P^T q columns 16kk .. 16kk+15 sit at TMEM column 64 (kk / 4) + 8 (kk % 4)
+                            umma_bf16_ts(tmem + kC, tmem + kA + (kk >> 2) * 64 + (kk & 3) * 8,
+                                         sdesc_sw128(do_addr + kk * 2048, kAtom, 1024), id_kn,
+                                         (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&sm.do_empty[st]);
+                    ++do_commits[st];
+                    // dK += dS^T Q (M = kv), dQ_part = dS K (M = q) into B
+                    if (!mbar_wait(&sm.ds_full, ph, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    {
+                        const uint32_t q_addr = smem_u32(sm.q[st][0]);
+#pragma unroll
+                        for (int kk = 0; kk < 128 / 16; ++kk)
+                            umma_bf16(tmem + kE, sdesc_sw128(ds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
+                                      sdesc_sw128(q_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < 128 / 16; ++kk)
+                            umma_bf16(tmem + kB, sdesc_sw128(ds_addr + kk * 2048, kAtom, 1024),
+                                      sdesc_sw128(k_addr + kk * 2048, kAtom, 1024), id_mn, kk > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&sm.dq_full);
+                    // next step: S^T over P^T (dV ran before it and the dS warps read
+                    // P^T before ds_full), then dP^T
+                    if (i + 1 < nsteps && !(issue_s(gi + 1) && issue_dp(gi + 1))) { ok = false; break; }
                 }
-                umma_commit(&sm.do_empty[st]);
-                ++do_commits[st];
-                // dK += dS^T Q(i) (M = kv), dQ_part = dS K (M = q) into B
-                if (!mbar_wait(&sm.ds_full, ph, abort_flag, a.status)) { ok = false; break; }
-                tc_fence_after();
-                {
-                    const uint32_t q_addr = smem_u32(sm.q[st][0]);
-#pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk)
-                        umma_bf16(tmem + kE, sdesc_sw128(ds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                                  sdesc_sw128(q_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < 128 / 16; ++kk)
-                        umma_bf16(tmem + kB, sdesc_sw128(ds_addr + kk * 2048, kAtom, 1024),
-                                  sdesc_sw128(k_addr + kk * 2048, kAtom, 1024), id_mn, kk > 0 ? 1u : 0u);
-                }
-                umma_commit(&sm.dq_full);
-                // next step: S^T(i+1) over P^T(i) (dV(i) ran before it and the dS warps
-                // read P^T(i) before ds_full(i)), then dP^T(i+1)
-                if (i + 1 < nsteps && !(issue_s(i + 1) && issue_dp(i + 1))) { ok = false; break; }
+                if (!ok) break;
+                umma_commit(&sm.kv_empty);   // K / V fully read: the next unit's may load
+                ++kv_commits;
             }
-            umma_commit(&sm.fin);
             umma_commit(&sm.drain);
             wait_drain(&sm.drain, 0);
             for (int s = 0; s < kQStages; ++s)
                 if (do_commits[s] > 0) wait_drain(&sm.do_empty[s], (do_commits[s] - 1) & 1);
+            if (kv_commits > 0) wait_drain(&sm.kv_empty, (kv_commits - 1) & 1);
         }
-    } else if (warp < kPWarps) {
-        // ------------------------------------------------------------ P warps
-        const int quarter = warp & 3, half = warp >> 2;
-        const int t = quarter * 32 + lane;                        // kv row = TMEM lane
-        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const int col0 = half * 64;                               // this warp's 64 q columns
-        const float sl2 = a.scale_log2;
-        const int kj = k0 + t;
-        const bool loader = half == 0;                            // loads the step's LSE column t
-        const int my_chunk = half;                                // dQ read-out chunk (d columns 32c..)
-        const bool reads_out = my_chunk < D / 64;
-        bool ok = true;
-        auto col_term = [&](int i) -> float {
-            const int h = g * group + i / nq;
-            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + t;
-            if (qi >= a.total_tokens) return 0.f;
-            return a.lse[static_cast<size_t>(h) * a.total_tokens + qi] * 1.4426950408889634f;
-        };
-        float nxt = loader ? col_term(0) : 0.f;
-        for (int i = 0; i < nsteps; ++i) {
-            const int h = g * group + i / nq;
-            const int q0 = tl.seg_start + (tl.t + i % nq) * kTile;
-            if (loader) {
-                sm.lse2[i & 1][t] = nxt;
-                mbar_arrive(&sm.cols_l[i & 1]);
-                if (i + 1 < nsteps) nxt = col_term(i + 1);
-            }
-            if (!warp_wait(&sm.cols_l[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-            const float *L2 = sm.lse2[i & 1] + col0;
-            // column col0 + c (q row q0 + col0 + c) is live for kv row kj iff kj <= q row < seg_end
-            const int c_lo = kj - q0 - col0, c_hi = tl.seg_end - q0 - col0;
-            const bool full = c_lo <= 0 && c_hi >= 64;
-            if (!warp_wait(&sm.s_full, i & 1, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            // P^T columns col0 + 32c .. +31 (bf16 pairs) go to TMEM columns col0 + 16c ..
-            // +15, inside the S^T columns this warp has already read itself.
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t sv[32];
-                tmem_ld32(tmem + lane_off + kA + col0 + c * 32, sv);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int col = c * 32 + 2 * e;
-                    float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - L2[col]);
-                    float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - L2[col + 1]);
-                    if (!full) {
-                        if (col < c_lo || col >= c_hi) p0 = 0.f;
-                        if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
-                    }
-                    pk[e] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tmem + lane_off + kA + col0 + c * 16, pk);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&sm.p_full);
-            // The Q(i-1) stage held this warp's staged dQ(i-1) chunk: once the TMA
-            // engine has read it (it had the whole P computation to do so) the
-            // stage goes back to the producer.
-            if (i > 0 && reads_out) {
-                if (lane == 0) {
-                    bulk_wait_group_read0();
-                    mbar_arrive(&sm.q_empty[(i - 1) % kQStages]);
-                }
-                __syncwarp();
-            }
-            // dQ(i) read-out of one [32 rows][32 cols] chunk, staged in this warp's
-            // slice of the Q(i) stage (free once dK(i) completed) in the 128-byte-
-            // swizzled layout and added by the TMA engine in the background.
-            if (!warp_wait(&sm.dq_full, i & 1, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            if (reads_out) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kB + my_chunk * 32, v);
-                tmem_wait_ld();
-                const uint8_t *stage = sm.q[i % kQStages][0] + (quarter + 4 * my_chunk) * 4096;
-                const uint32_t stage_addr = smem_u32(stage);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    st_shared_v4(stage_addr + lane * 128 + ((e ^ (lane & 7)) << 4), v[4 * e], v[4 * e + 1],
-                                 v[4 * e + 2], v[4 * e + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (q0 + quarter * 32 < tl.seg_end)   // skip a chunk of padding rows only
-                        tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, h * (D / 32) + my_chunk);
-                    bulk_commit_group();
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&sm.dq_free);
-        }
-        if (lane == 0) bulk_wait_group0();     // every reduce of this warp has landed
-        __syncwarp();
-        (void)ok;
     } else {
-        // ------------------------------------------------------------ dS warps
-        const int w = warp - kPWarps;
+        // ------------------------------------------------------------ compute warps
+        // One body, instantiated for the P warps and for the dS warps.
+        auto compute = [&](auto role) {
+        constexpr bool is_p = decltype(role)::value;
+        const int w = is_p ? warp : warp - kPWarps;
         const int quarter = w & 3, half = w >> 2;
         const int t = quarter * 32 + lane;                        // kv row / q row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t ds_addr = smem_u32(sm.ds[0]);
         const int col0 = half * 64;                               // this warp's 64 q columns
-        const int kj = k0 + t;
-        const bool loader = half == 0;                            // loads the step's D column t
-        const int my_chunk = D / 64 + half;                       // dQ read-out chunk, if any
-        const bool reads_out = my_chunk < D / 32;
-        bool ok = true;
-        auto col_term = [&](int i) -> float {
-            const int h = g * group + i / nq;
-            const int qi = tl.seg_start + (tl.t + i % nq) * kTile + t;
+        const float sl2 = a.scale_log2;
+        const uint32_t ds_addr = smem_u32(sm.ds[0]);
+        const bool loader = half == 0;                            // loads the step's LSE / D column t
+        // dQ read-out chunk (d columns 32 c ..): P warps take the first D / 64, dS warps the rest
+        const int my_chunk = is_p ? half : D / 64 + half;
+        const bool reads_out = is_p ? my_chunk < D / 64 : my_chunk < D / 32;
+        auto col_term = [&](const int4 &u, int i) -> float {
+            const int nq = seg_tiles(u) - u.w;
+            const int h = u.x * group + i / nq;
+            const int qi = u.y + (u.w + i % nq) * kTile + t;
             if (qi >= a.total_tokens) return 0.f;
-            return a.delta[static_cast<size_t>(h) * a.total_tokens + qi];
+            const size_t x = static_cast<size_t>(h) * a.total_tokens + qi;
+            return is_p ? a.lse[x] * 1.4426950408889634f : a.delta[x];
         };
-        float nxt = loader ? col_term(0) : 0.f;
-        for (int i = 0; i < nsteps; ++i) {
-            const int h = g * group + i / nq;
-            const int q0 = tl.seg_start + (tl.t + i % nq) * kTile;
-            const uint32_t ph = i & 1;
-            if (loader) {
-                sm.delta[i & 1][t] = nxt;
-                mbar_arrive(&sm.cols_d[i & 1]);
-                if (i + 1 < nsteps) nxt = col_term(i + 1);
-            }
-            if (!warp_wait(&sm.cols_d[i & 1], (i >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-            const float *DD = sm.delta[i & 1] + col0;
-            // dS^T = P^T * (dP^T - D); P^T read back from TMEM (bf16), masked entries are 0
-            if (!warp_wait(&sm.dp_full, ph, abort_flag, a.status)) { ok = false; break; }
-            if (!warp_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            // This warp's slice of the dS buffer held its staged dQ(i-1) chunk: it is
-            // reusable once the TMA engine has read it (dK(i-1) / dQ(i-1), its other
-            // readers, completed before dq_full(i-1)). dP(i) ran meanwhile.
-            if (i > 0 && reads_out) {
-                if (lane == 0) bulk_wait_group_read0();
-                __syncwarp();
-            }
+        // Stages one [32 rows][32 cols] chunk of dQ (TMEM region B) in the 128-byte-
+        // swizzled layout and lets the TMA engine add it into the accumulator in
+        // the background. Rows past the segment carry exact zeros.
+        auto dq_readout = [&](const uint8_t *stage, int q0, int seg_end, int h) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + kB + my_chunk * 32, v);
+            tmem_wait_ld();
+            const uint32_t stage_addr = smem_u32(stage);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t dp[32], pv[16];
-                tmem_ld32(tmem + lane_off + kB + col0 + c * 32, dp);
-                tmem_ld16(tmem + lane_off + kA + col0 + c * 16, pv);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int col = c * 32 + 2 * e;
-                    const float d0 = bf16_lo(pv[e]) * (__uint_as_float(dp[2 * e]) - DD[col]);
-                    const float d1 = bf16_hi(pv[e]) * (__uint_as_float(dp[2 * e + 1]) - DD[col + 1]);
-                    pk[e] = pack_bf16x2(d0, d1);
-                }
-                // row t, q columns col0 + 32c .. +31: atom `half`, 16-byte chunks 4c .. 4c+3
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    const int chunk = c * 4 + v4;
-                    st_shared_v4(ds_addr + half * kAtom + t * 128 + ((chunk ^ (t & 7)) << 4), pk[4 * v4],
-                                 pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-                }
-            }
+            for (int e = 0; e < 8; ++e)
+                st_shared_v4(stage_addr + lane * 128 + ((e ^ (lane & 7)) << 4), v[4 * e], v[4 * e + 1], v[4 * e + 2],
+                             v[4 * e + 3]);
             fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&sm.ds_full);
-
-            // dQ(i) read-out of one [32 rows][32 cols] chunk, staged in this warp's
-            // slice of the dS buffer (free: dK(i) and dQ(i) completed) in the 128-
-            // byte-swizzled layout and added by the TMA engine in the background.
-            // Rows past the segment carry exact zeros.
-            if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
-            tc_fence_after();
-            if (reads_out) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + kB + my_chunk * 32, v);
-                tmem_wait_ld();
-                const uint8_t *stage = sm.ds[0] + (quarter + 4 * half) * 4096;
-                const uint32_t stage_addr = smem_u32(stage);
+            __syncwarp();
+            if (lane == 0) {
+                if (q0 + quarter * 32 < seg_end)   // skip a chunk of padding rows only
+                    tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, h * (D / 32) + my_chunk);
+                bulk_commit_group();
+            }
+        };
+        // dV (P warps) or dK (dS warps) rows of the unit's kv tile: this warp's
+        // 32 rows, d columns [half * D/2, half * D/2 + D/2).
+        auto store_rows = [&](const int4 &u) {
+            const int kj = u.y + u.w * kTile + t;
+            const bool live = kj < u.z;
+            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + u.x) * D + half * (D / 2);
+            const uint32_t col = (is_p ? kC : kE) + half * (D / 2);
+            const float mul = is_p ? 1.f : a.scale;
+            void *base = is_p ? a.dv : a.dk;
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    st_shared_v4(stage_addr + lane * 128 + ((e ^ (lane & 7)) << 4), v[4 * e], v[4 * e + 1],
-                                 v[4 * e + 2], v[4 * e + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (q0 + quarter * 32 < tl.seg_end)   // skip a chunk of padding rows only
-                        tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, h * (D / 32) + my_chunk);
-                    bulk_commit_group();
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_off + col + c * 32, v);
+                tmem_wait_ld();
+                if (!live) continue;
+                if (a.grad_fp32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base) + orow + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        dst[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                                             __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + orow + c * 32);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                            pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                            pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                            pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&sm.dq_free);
+        };
+
+        int4 cur;
+        bool ok = warp_unit(0, cur);
+        float nxt = (ok && loader && cur.x >= 0) ? col_term(cur, 0) : 0.f;
+        int gi = 0;
+        for (int it = 0; ok && cur.x >= 0; ++it) {
+            const int nq = seg_tiles(cur) - cur.w;
+            const int nsteps = group * nq;
+            const int kj = cur.y + cur.w * kTile + t;
+            for (int i = 0; i < nsteps; ++i, ++gi) {
+                const int h = cur.x * group + i / nq;
+                const int q0 = cur.y + (cur.w + i % nq) * kTile;
+                const uint32_t ph = gi & 1;
+                float *colbuf = is_p ? sm.lse2[gi & 1] : sm.delta[gi & 1];
+                uint64_t *colbar = is_p ? &sm.cols_l[gi & 1] : &sm.cols_d[gi & 1];
+                if (loader) {
+                    colbuf[t] = nxt;
+                    mbar_arrive(colbar);
+                    if (i + 1 < nsteps) nxt = col_term(cur, i + 1);
+                }
+                if (!warp_wait(colbar, (gi >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                const float *CC = colbuf + col0;
+                if constexpr (is_p) {
+                    // P^T = exp(S^T * scale - LSE); column col0 + c (q row q0 + col0 + c)
+                    // is live for kv row kj iff kj <= q row < seg_end
+                    const int c_lo = kj - q0 - col0, c_hi = cur.z - q0 - col0;
+                    const bool full = c_lo <= 0 && c_hi >= 64;
+                    if (!warp_wait(&sm.s_full, ph, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    // P^T columns col0 + 32c .. +31 (bf16 pairs) go to TMEM columns col0 + 16c ..
+                    // +15, inside the S^T columns this warp has already read itself.
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t sv[32];
+                        tmem_ld32(tmem + lane_off + kA + col0 + c * 32, sv);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int col = c * 32 + 2 * e;
+                            float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - CC[col]);
+                            float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - CC[col + 1]);
+                            if (!full) {
+                                if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                            }
+                            pk[e] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(tmem + lane_off + kA + col0 + c * 16, pk);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&sm.p_full);
+                    // The previous Q stage held this warp's staged dQ chunk: once the TMA
+                    // engine has read it (it had the whole P computation to do so) the
+                    // stage goes back to the producer.
+                    if (gi > 0 && reads_out) {
+                        if (lane == 0) {
+                            bulk_wait_group_read0();
+                            mbar_arrive(&sm.q_empty[(gi - 1) % kQStages]);
+                        }
+                        __syncwarp();
+                    }
+                } else {
+                    // dS^T = P^T * (dP^T - D); P^T read back from TMEM (bf16), masked entries are 0
+                    if (!warp_wait(&sm.dp_full, ph, abort_flag, a.status)) { ok = false; break; }
+                    if (!warp_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    // This warp's slice of the dS buffer held its staged dQ chunk of the
+                    // previous step: reusable once the TMA engine has read it (the dK /
+                    // dQ MMAs, its other readers, completed before that step's dq_full).
+                    if (gi > 0 && reads_out) {
+                        if (lane == 0) bulk_wait_group_read0();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t dp[32], pv[16];
+                        tmem_ld32(tmem + lane_off + kB + col0 + c * 32, dp);
+                        tmem_ld16(tmem + lane_off + kA + col0 + c * 16, pv);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int col = c * 32 + 2 * e;
+                            const float d0 = bf16_lo(pv[e]) * (__uint_as_float(dp[2 * e]) - CC[col]);
+                            const float d1 = bf16_hi(pv[e]) * (__uint_as_float(dp[2 * e + 1]) - CC[col + 1]);
+                            pk[e] = pack_bf16x2(d0, d1);
+                        }
+                        // row t, q columns col0 + 32c .. +31: atom `half`, 16-byte chunks 4c .. 4c+3
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            const int chunk = c * 4 + v4;
+                            st_shared_v4(ds_addr + half * kAtom + t * 128 + ((chunk ^ (t & 7)) << 4), pk[4 * v4],
+                                         pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&sm.ds_full);
+                }
+                // dQ read-out of one chunk, staged in this warp's slice of the spent
+                // Q stage (P warps: Q was last read by dK, complete at dq_full) or of
+                // the dS buffer (dS warps: dK / dQ, its readers, complete at dq_full).
+                if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                if (reads_out) {
+                    const uint8_t *stage = is_p ? sm.q[gi % kQStages][0] + (quarter + 4 * my_chunk) * 4096
+                                                : sm.ds[0] + (quarter + 4 * half) * 4096;
+                    dq_readout(stage, q0, cur.z, h);
+                }
+                tc_fence_before();
+                mbar_arrive(&sm.dq_free);
+            }
+            if (!ok) break;
+            // Every MMA of the unit has completed (its last dq_full). Take the next
+            // unit and start its first column load, then read out this unit's dV / dK;
+            // the next unit's first dV / dK MMAs wait for p_full / ds_full, which
+            // these warps signal only after the read-out.
+            int4 nu;
+            if (!warp_unit(it + 1, nu)) { ok = false; break; }
+            if (loader && nu.x >= 0) nxt = col_term(nu, 0);
+            store_rows(cur);
+            cur = nu;
         }
         if (lane == 0) bulk_wait_group0();     // every reduce of this warp has landed
         __syncwarp();
-        // dK, dV rows of this tile, d columns [half * D/2, half * D/2 + D/2)
-        if (ok && warp_wait(&sm.fin, 0, abort_flag, a.status)) {
-            tc_fence_after();
-            const bool live = kj < tl.seg_end;
-            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + g) * D + half * (D / 2);
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = (which ? kE : kC) + half * (D / 2);
-                const float mul = which ? a.scale : 1.f;
-                void *base = which ? a.dk : a.dv;
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_off + col + c * 32, v);
-                    tmem_wait_ld();
-                    if (!live) continue;
-                    if (a.grad_fp32) {
-                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base) + orow + c * 32);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            dst[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
-                                                 __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + orow + c * 32);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
-                                                pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
-                                                pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
-                                                pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
-                    }
-                }
-            }
-        }
+        };
+        if (warp < kPWarps) compute(std::true_type{});
+        else compute(std::false_type{});
     }
 
     tc_fence_before();
@@ -592,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t stream)
+cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t max_units, cudaStream_t stream)
 {
     const int T = a.total_tokens;
     const long long rows = static_cast<long long>(T) * a.Hq;
@@ -608,13 +648,15 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t 
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    AttnBwdArgs a2 = a;
-    a2.grid_tiles = static_cast<int32_t>(grid_tiles);
-    const int64_t grid = grid_tiles * a.Hkv;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // Persistent: one CTA per SM takes work units from the shared counter.
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int64_t grid = max_units * a.Hkv;
+    if (grid > sms) grid = sms;
     if (grid > 0) {
         prof_begin(kProfAttnBwd, stream);
-        attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a2);
+        attn_bwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
         prof_end(kProfAttnBwd, stream);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -628,10 +670,11 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t grid_tiles, cudaStream_t 
 
 }  // namespace
 
-cudaError_t launch_attn_bwd(const AttnBwdArgs &a, int head_dim, int64_t grid_tiles, cudaStream_t stream)
+// max_units: upper bound of the number of kv tiles of one kv head.
+cudaError_t launch_attn_bwd(const AttnBwdArgs &a, int head_dim, int64_t max_units, cudaStream_t stream)
 {
-    if (head_dim == 64) return launch_bwd_d<64>(a, grid_tiles, stream);
-    if (head_dim == 128) return launch_bwd_d<128>(a, grid_tiles, stream);
+    if (head_dim == 64) return launch_bwd_d<64>(a, max_units, stream);
+    if (head_dim == 128) return launch_bwd_d<128>(a, max_units, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -124,15 +124,15 @@ struct AttnBwdArgs {
     int grad_fp32;
     const Tile *tiles;
     const int32_t *tile_count;
+    int32_t *work_counter;  // next work unit (zeroed by the scheduler kernel)
     int *status;
     int32_t total_tokens;
     int32_t Hq, Hkv;
-    int32_t grid_tiles;  // tile slots per kv head in the grid (blockIdx = kv head * grid_tiles + tile)
     float scale_log2;
     float scale;
 };
 
-cudaError_t launch_attn_bwd(const AttnBwdArgs &a, int head_dim, int64_t grid_tiles,
+cudaError_t launch_attn_bwd(const AttnBwdArgs &a, int head_dim, int64_t max_units,
                             cudaStream_t stream);
 
 }  // namespace spd
