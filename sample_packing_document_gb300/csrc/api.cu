@@ -72,13 +72,13 @@ EncodeTiled encode_fn()
 
 // Tensor map over a [T, H, D] bf16 array: dims (D, H, T), box (64, 1, 128),
 // 128-byte swizzle; rows past T read as zero.
-int make_map(CUtensorMap *m, const void *base, int64_t T, int H, int D)
+int make_map(CUtensorMap *m, const void *base, int64_t T, int H, int D, int box_rows = kTile)
 {
     EncodeTiled f = encode_fn();
     if (!f) return SPD_ERR_CUDA;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2};
-    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -335,6 +335,11 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.dk = dk;
     a.dv = dv;
     a.grad_fp32 = grad_dtype;
+    a.store_tma = grad_dtype == 0 && head_dim == 128;
+    if (a.store_tma) {
+        if ((rc = make_map(&a.tm_dk, dk, total_tokens, Hkv, head_dim, 32)) != SPD_OK) return rc;
+        if ((rc = make_map(&a.tm_dv, dv, total_tokens, Hkv, head_dim, 32)) != SPD_OK) return rc;
+    }
     a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
     a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
     a.work_counter = reinterpret_cast<int32_t *>(base) + 2;

@@ -44,7 +44,11 @@
 namespace spd {
 namespace {
 
-constexpr int kThreads = 576;        // 16 compute warps + producer + MMA issuer
+constexpr int kThreads = 640;        // 16 compute warps (4 warpgroups) + producer + MMA issuer + 2 idle warps
+// Register split (setmaxnreg): the launch gives 96 per thread (640 x 96 = 61440); the
+// warpgroup of the producer / MMA issuer drops to 64 and the four compute
+// warpgroups rise to 104: 4 x 128 x 104 + 128 x 64 = 61440.
+constexpr uint32_t kComputeRegs = 104, kControlRegs = 64;
 constexpr int kPWarps = 8, kDsWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;
@@ -180,6 +184,76 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
     }
 }
 
+// dV (P warps, IS_P) or dK (dS warps) rows of a finished unit's kv tile: the
+// calling warp's 32 rows (TMEM lanes 32 quarter ..), d columns [half * D/2,
+// half * D/2 + D/2), read from TMEM at `acc`. With bf16 grads and d = 128, a
+// quarter that lies wholly inside the segment is converted into the warp's
+// staging slot (free once the TMA engine has read the unit's last dQ chunk from
+// it) and leaves in one TMA store, so the HBM writes are whole lines; a quarter
+// that reaches past the segment end is written by plain stores of its live rows
+// (a box must not touch the next segment). Called once per unit.
+template <int D, bool IS_P>
+__device__ __forceinline__ void store_acc_rows(const AttnBwdArgs &a, uint32_t acc, int4 u, int quarter, int half,
+                                            const uint8_t *slot)
+{
+    const int lane = threadIdx.x & 31;
+    const int row0 = u.y + u.w * kTile + quarter * 32;
+    const int kj = row0 + lane;
+    const float mul = IS_P ? 1.f : a.scale;
+    if (D == 128 && a.store_tma && row0 + 32 <= u.z) {
+        const uint32_t slot_addr = smem_u32(slot);
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(acc + c * 32, v);
+            tmem_wait_ld();
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                w[e] = pack_bf16x2(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+            // row `lane`, d columns 32c .. 32c+31: 16-byte chunks 4c .. 4c+3, 128-byte swizzle
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+                st_shared_v4(slot_addr + lane * 128 + (((c * 4 + v4) ^ (lane & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
+                             w[4 * v4 + 2], w[4 * v4 + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_3d(IS_P ? &a.tm_dv : &a.tm_dk, slot, half * 64, u.x, row0);
+            bulk_commit_group();
+        }
+        return;
+    }
+    const bool live = kj < u.z;
+    const size_t orow = (static_cast<size_t>(kj) * a.Hkv + u.x) * D + half * (D / 2);
+    void *base = IS_P ? a.dv : a.dk;
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[32];
+        tmem_ld32(acc + c * 32, v);
+        tmem_wait_ld();
+        if (!live) continue;
+        if (a.grad_fp32) {
+            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base) + orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                dst[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
+                                     __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
+        } else {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + orow + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
+                                    pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
+                                    pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
+                                    pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
+        }
+    }
+}
+
 // ------------------------------------------------------------------ main kernel
 __device__ __forceinline__ int seg_tiles(const int4 &u) { return (u.z - u.y + kTile - 1) / kTile; }
 
@@ -227,6 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         tmem_relinquish();
     }
     if (warp == 16 && lane == 0) {
+        if (a.store_tma) {
+            tma_prefetch_desc(&a.tm_dk);
+            tma_prefetch_desc(&a.tm_dv);
+        }
         tma_prefetch_desc(&a.tm_q);
         tma_prefetch_desc(&a.tm_k);
         tma_prefetch_desc(&a.tm_v);
@@ -251,6 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         return true;
     };
 
+    if (warp >= 16) {
+    setmaxnreg_dec<kControlRegs>();
     if (warp == 16) {
         // ------------------------------------------------------------ producer
         // Takes work units (kv head, kv tile) from the shared counter in list
@@ -417,7 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 if (do_commits[s] > 0) wait_drain(&sm.do_empty[s], (do_commits[s] - 1) & 1);
             if (kv_commits > 0) wait_drain(&sm.kv_empty, (kv_commits - 1) & 1);
         }
+    }
     } else {
+        setmaxnreg_inc<kComputeRegs>();
         // ------------------------------------------------------------ compute warps
         // One body, instantiated for the P warps and for the dS warps.
         auto compute = [&](auto role) {
@@ -461,37 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 bulk_commit_group();
             }
         };
-        // dV (P warps) or dK (dS warps) rows of the unit's kv tile: this warp's
-        // 32 rows, d columns [half * D/2, half * D/2 + D/2).
-        auto store_rows = [&](const int4 &u) {
-            const int kj = u.y + u.w * kTile + t;
-            const bool live = kj < u.z;
-            const size_t orow = (static_cast<size_t>(kj) * a.Hkv + u.x) * D + half * (D / 2);
-            const uint32_t col = (is_p ? kC : kE) + half * (D / 2);
-            const float mul = is_p ? 1.f : a.scale;
-            void *base = is_p ? a.dv : a.dk;
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_off + col + c * 32, v);
-                tmem_wait_ld();
-                if (!live) continue;
-                if (a.grad_fp32) {
-                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(base) + orow + c * 32);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[e] = make_float4(__uint_as_float(v[4 * e]) * mul, __uint_as_float(v[4 * e + 1]) * mul,
-                                             __uint_as_float(v[4 * e + 2]) * mul, __uint_as_float(v[4 * e + 3]) * mul);
-                } else {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(base) + orow + c * 32);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]) * mul, __uint_as_float(v[8 * e + 1]) * mul),
-                                            pack_bf16x2(__uint_as_float(v[8 * e + 2]) * mul, __uint_as_float(v[8 * e + 3]) * mul),
-                                            pack_bf16x2(__uint_as_float(v[8 * e + 4]) * mul, __uint_as_float(v[8 * e + 5]) * mul),
-                                            pack_bf16x2(__uint_as_float(v[8 * e + 6]) * mul, __uint_as_float(v[8 * e + 7]) * mul));
-                }
-            }
+        auto store_rows = [&](const int4 &u, int gs_last) {
+            const uint8_t *slot = (is_p ? sm.q[gs_last % kQStages][0] : sm.ds[0]) + (quarter + 4 * half) * 4096;
+            store_acc_rows<D, is_p>(a, tmem + lane_off + (is_p ? kC : kE) + half * (D / 2), u, quarter, half, slot);
         };
 
         int4 cur;
@@ -615,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             int4 nu;
             if (!warp_unit(it + 1, nu)) { ok = false; break; }
             if (loader && nu.x >= 0) nxt = col_term(nu, 0);
-            store_rows(cur);
+            store_rows(cur, gi - 1);
             cur = nu;
         }
         if (lane == 0) bulk_wait_group0();     // every reduce of this warp has landed

@@ -115,6 +115,7 @@ cudaError_t launch_attn_fwd(const AttnFwdArgs &a, int head_dim, int64_t grid_til
 struct AttnBwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
     CUtensorMap tm_dqacc;  // fp32 dQ accumulator as [Hq * d / 32][T][32]
+    CUtensorMap tm_dk, tm_dv;  // bf16 dK / dV, boxes of 64 d x 32 rows (used when store_tma)
     const uint16_t *out;
     const uint16_t *dout;
     const float *lse;
@@ -122,6 +123,7 @@ struct AttnBwdArgs {
     float *delta;    // [Hq, total_tokens] fp32
     void *dq, *dk, *dv;
     int grad_fp32;
+    int store_tma;   // dK / dV rows leave through TMA stores (bf16 grads, d = 128)
     const Tile *tiles;
     const int32_t *tile_count;
     int32_t *work_counter;  // next work unit (zeroed by the scheduler kernel)
