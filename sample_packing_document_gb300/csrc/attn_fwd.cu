@@ -10,11 +10,12 @@
 // only when the max grows by more than 2^8, which keeps every partial value
 // within fp32 / bf16 range and leaves the result exact up to rounding).
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads; warps 10-11 only complete the third warpgroup):
 //   warps 0-3 / 4-7  softmax of tile A / B: thread r owns q row r (TMEM lane
-//                    r). Reads S_X from TMEM, writes P_X as bf16 back into the
-//                    first 64 columns of S_X's TMEM region, rescales O_X in
-//                    TMEM when needed, final normalisation and stores.
+//                    r). Reads the whole S_X row from TMEM into registers once,
+//                    writes P_X as bf16 back into the first 64 columns of S_X's
+//                    TMEM region, rescales O_X in TMEM when needed, final
+//                    normalisation and stores.
 //   warp 8           TMA producer: takes the next work unit, loads Q_A, Q_B and
 //                    streams the K / V tiles through a 2-stage ring that runs
 //                    on across units.
@@ -34,7 +35,12 @@ namespace spd {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+// Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 = 64512);
+// the warpgroup of the producer / MMA issuer drops to 72 and the two softmax
+// warpgroups rise to 216 (2 x 128 x 216 + 128 x 72 = 64512), enough to keep a
+// whole 128-column S row in registers.
+constexpr uint32_t kSoftmaxRegs = 216, kControlRegs = 72;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;  // bytes of one [128 rows][64 bf16] swizzled atom
 
@@ -80,6 +86,21 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// As umma_bf16_ts with B given as a base descriptor plus a start-address step
+// (bytes / 16) added inside the instruction block.
+__device__ __forceinline__ void umma_bf16_ts_step(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t b_step,
+                                                  uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 bd, bs;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "cvt.u64.u32 bs, %3;\n\t"
+        "add.s64 bd, %2, bs;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_base), "r"(b_step), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -146,6 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int units_per_head = *a.tile_count;
     const int total_units = units_per_head * a.Hq;
 
+    if (warp >= 8) {
+    setmaxnreg_dec<kControlRegs>();
     if (warp == 8) {
         // ------------------------------------------------------------ producer
         // Takes work units from the shared counter in list order: head-major
@@ -223,13 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const int n_tile0 = us.tA + 1, n_tile1 = us.has_b ? us.tA + 2 : 0;  // kv tiles each q tile reads
                 int s_left = n_tile0 + n_tile1;   // S MMAs of this unit still to issue
                 auto issue_s = [&](int x, int j) {
-                    const uint32_t q_addr = smem_u32(sm.q[x][0]);
-                    const uint32_t k_addr = smem_u32(sm.k[(kv_iter + j) % kStages][0]);
+                    // descriptors of the k-steps differ only in the start address (low field)
+                    const uint64_t qd = sdesc_sw128(smem_u32(sm.q[x][0]), 16, 1024);
+                    const uint64_t kd = sdesc_sw128(smem_u32(sm.k[(kv_iter + j) % kStages][0]), 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                        umma_bf16(tmem + x * 128, sdesc_sw128(q_addr + off, 16, 1024),
-                                  sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                        const uint32_t off16 = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+                        umma_bf16_step(tmem + x * 128, qd, kd, off16, off16, idesc_s, kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&sm.s_full[x]);
                     if (--s_left == 0) {             // Q_A / Q_B fully read: next unit may load
@@ -238,11 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 };
                 auto issue_pv = [&](int x, int j) {
-                    const uint32_t v_addr = smem_u32(sm.v[(kv_iter + j) % kStages][0]);
+                    const uint64_t vd = sdesc_sw128(smem_u32(sm.v[(kv_iter + j) % kStages][0]), kAtom, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 128 / 16; ++kk)
-                        umma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8,
-                                     sdesc_sw128(v_addr + kk * 2048, kAtom, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts_step(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, vd, kk * (2048 >> 4), idesc_o,
+                                          (j > 0 || kk > 0) ? 1u : 0u);
                 };
                 ok = mbar_wait(&sm.q_full, it & 1, abort_flag, a.status) &&
                      mbar_wait(&sm.k_full[kv_iter % kStages], (kv_iter / kStages) & 1, abort_flag, a.status);
@@ -297,7 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (empty_commits[s] > 0) wait_drain(&sm.kv_empty[s], (empty_commits[s] - 1) & 1);
             if (q_commits > 0) wait_drain(&sm.q_empty, (q_commits - 1) & 1);
         }
+    }
     } else {
+        setmaxnreg_inc<kSoftmaxRegs>();
         // ------------------------------------------------------------ softmax
         const int x = warp >> 2;                      // 0: tile A, 1: tile B
         const int r = threadIdx.x & 127;              // q row within the tile = TMEM lane
@@ -324,24 +349,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 ++s_cnt;
                 tc_fence_after();
                 const bool diag = (j == tX);
-                // pass 1: row max, 64 columns per TMEM round trip, 8 independent chains
+                // The whole S row (128 columns) is read once into registers.
+                uint32_t sv[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32(tmem + lane_off + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+                tmem_wait_ld();
+                // row max, 8 independent chains
                 float mxs[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) mxs[e] = -INFINITY;
+                if (diag) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t sv[64];
-                    tmem_ld32(tmem + lane_off + s_col + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-                    tmem_ld32(tmem + lane_off + s_col + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-                    tmem_wait_ld();
-                    if (diag) {
+                    for (int e = 0; e < 128; ++e)
+                        if (e <= r) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
+                } else {
 #pragma unroll
-                        for (int e = 0; e < 64; ++e)
-                            if (c * 64 + e <= r) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 64; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
-                    }
+                    for (int e = 0; e < 128; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
                 }
                 const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
                                        fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
@@ -365,23 +389,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     l *= alpha;
                     m = m_use;
                 }
-                // pass 2: P = 2^(S * scale * log2 e - m), written as bf16 over the
-                // first 64 columns of S_X's region; P columns 32c..32c+31 only cover
-                // S columns already read.
+                // P = 2^(S * scale * log2 e - m), written as bf16 over the first 64
+                // columns of S_X's region (already in registers).
                 float sums[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    uint32_t sv[32];
-                    tmem_ld32(tmem + lane_off + s_col + c * 32, sv);
-                    tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - m);
-                        float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - m);
+                        const int col = c * 32 + 2 * e;
+                        float p0 = ex2(__uint_as_float(sv[col]) * sl2 - m);
+                        float p1 = ex2(__uint_as_float(sv[col + 1]) * sl2 - m);
                         if (diag) {
-                            if (c * 32 + 2 * e > r) p0 = 0.f;
-                            if (c * 32 + 2 * e + 1 > r) p1 = 0.f;
+                            if (col > r) p0 = 0.f;
+                            if (col + 1 > r) p1 = 0.f;
                         }
                         sums[e & 3] += p0 + p1;
                         pk[e] = pack_bf16x2(p0, p1);

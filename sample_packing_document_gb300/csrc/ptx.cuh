@@ -309,6 +309,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// D[tmem] (+)= A[smem] * B[smem] with both descriptors given as a base plus a
+// start-address step (bytes / 16) added inside the instruction block, so an
+// unrolled k-loop keeps only the two base descriptors live.
+__device__ __forceinline__ void umma_bf16_step(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t a_step,
+                                               uint32_t b_step, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd, as, bs;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "cvt.u64.u32 as, %3;\n\t"
+        "cvt.u64.u32 bs, %4;\n\t"
+        "add.s64 ad, %1, as;\n\t"
+        "add.s64 bd, %2, bs;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_base), "l"(b_base), "r"(a_step), "r"(b_step), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, dense.
 //   a_mn / b_mn: 0 = K-major, 1 = MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn)
