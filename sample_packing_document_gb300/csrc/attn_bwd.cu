@@ -89,19 +89,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, w);
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, bf16) sits in TMEM, one row per
-// lane, two K elements per 32-bit column.
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -407,20 +394,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             constexpr uint32_t id_ss = idesc_bf16(128, 128, 0, 0);  // S^T, dP^T
             constexpr uint32_t id_kn = idesc_bf16(128, D, 0, 1);    // dV (A in TMEM), dK
             constexpr uint32_t id_mn = idesc_bf16(128, D, 1, 1);    // dQ
-            const uint32_t k_addr = smem_u32(sm.k[0]), v_addr = smem_u32(sm.v[0]);
-            const uint32_t ds_addr = smem_u32(sm.ds[0]);
+            // base descriptors; the k-steps add a start-address step inside the MMA block
+            const uint64_t kd_k = sdesc_sw128(smem_u32(sm.k[0]), 16, 1024);      // K, K-major (S^T A operand)
+            const uint64_t kd_v = sdesc_sw128(smem_u32(sm.v[0]), 16, 1024);      // V, K-major (dP^T A operand)
+            const uint64_t kd_mn = sdesc_sw128(smem_u32(sm.k[0]), kAtom, 1024);  // K, MN-major (dQ B operand)
+            const uint64_t dsd_k = sdesc_sw128(smem_u32(sm.ds[0]), 16, 1024);    // dS^T, K-major (dK A operand)
+            const uint64_t dsd_mn = sdesc_sw128(smem_u32(sm.ds[0]), kAtom, 1024); // dS, MN-major (dQ A operand)
             int do_commits[kQStages] = {};
             int kv_commits = 0;
             auto issue_s = [&](int gs) -> bool {   // S^T = K Q^T into A
                 const int st = gs % kQStages;
                 if (!mbar_wait(&sm.q_full[st], (gs / kQStages) & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
-                const uint32_t q_addr = smem_u32(sm.q[st][0]);
+                const uint64_t qd = sdesc_sw128(smem_u32(sm.q[st][0]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    umma_bf16(tmem + kA, sdesc_sw128(k_addr + off, 16, 1024), sdesc_sw128(q_addr + off, 16, 1024),
-                              id_ss, kk > 0 ? 1u : 0u);
+                    const uint32_t step = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+                    umma_bf16_step(tmem + kA, kd_k, qd, step, step, id_ss, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&sm.s_full);
                 return true;
@@ -430,12 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 if (!mbar_wait(&sm.do_full[st], (gs / kQStages) & 1, abort_flag, a.status)) return false;
                 if (gs > 0 && !mbar_wait(&sm.dq_free, (gs - 1) & 1, abort_flag, a.status)) return false;
                 tc_fence_after();
-                const uint32_t do_addr = smem_u32(sm.dout[st][0]);
+                const uint64_t dod = sdesc_sw128(smem_u32(sm.dout[st][0]), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kAtom + (kk & 3) * 32;
-                    umma_bf16(tmem + kB, sdesc_sw128(v_addr + off, 16, 1024), sdesc_sw128(do_addr + off, 16, 1024),
-                              id_ss, kk > 0 ? 1u : 0u);
+                    const uint32_t step = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+                    umma_bf16_step(tmem + kB, kd_v, dod, step, step, id_ss, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(&sm.dp_full);
                 return true;
@@ -458,13 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     if (!mbar_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
                     {
-                        const uint32_t do_addr = smem_u32(sm.dout[st][0]);
+                        const uint64_t dod = sdesc_sw128(smem_u32(sm.dout[st][0]), kAtom, 1024);
 #pragma unroll
                         for (int kk = 0; kk < 128 / 16; ++kk)
                             // P^T q columns 16kk .. 16kk+15 sit at TMEM column 64 (kk / 4) + 8 (kk % 4)
-                            umma_bf16_ts(tmem + kC, tmem + kA + (kk >> 2) * 64 + (kk & 3) * 8,
-                                         sdesc_sw128(do_addr + kk * 2048, kAtom, 1024), id_kn,
-                                         (i > 0 || kk > 0) ? 1u : 0u);
+                            umma_bf16_ts_step(tmem + kC, tmem + kA + (kk >> 2) * 64 + (kk & 3) * 8, dod,
+                                              kk * (2048 >> 4), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&sm.do_empty[st]);
                     ++do_commits[st];
@@ -472,15 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     if (!mbar_wait(&sm.ds_full, ph, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
                     {
-                        const uint32_t q_addr = smem_u32(sm.q[st][0]);
+                        const uint64_t qd_mn = sdesc_sw128(smem_u32(sm.q[st][0]), kAtom, 1024);
 #pragma unroll
                         for (int kk = 0; kk < 128 / 16; ++kk)
-                            umma_bf16(tmem + kE, sdesc_sw128(ds_addr + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024),
-                                      sdesc_sw128(q_addr + kk * 2048, kAtom, 1024), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
+                            umma_bf16_step(tmem + kE, dsd_k, qd_mn, ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4,
+                                           kk * (2048 >> 4), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                         for (int kk = 0; kk < 128 / 16; ++kk)
-                            umma_bf16(tmem + kB, sdesc_sw128(ds_addr + kk * 2048, kAtom, 1024),
-                                      sdesc_sw128(k_addr + kk * 2048, kAtom, 1024), id_mn, kk > 0 ? 1u : 0u);
+                            umma_bf16_step(tmem + kB, dsd_mn, kd_mn, kk * (2048 >> 4), kk * (2048 >> 4), id_mn,
+                                           kk > 0 ? 1u : 0u);
                     }
                     umma_commit(&sm.dq_full);
                     // next step: S^T over P^T (dV ran before it and the dS warps read

@@ -76,34 +76,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, w);
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, bf16) sits in TMEM, one row per
-// lane, two K elements per 32-bit column.
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// As umma_bf16_ts with B given as a base descriptor plus a start-address step
-// (bytes / 16) added inside the instruction block.
-__device__ __forceinline__ void umma_bf16_ts_step(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t b_step,
-                                                  uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 bd, bs;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "cvt.u64.u32 bs, %3;\n\t"
-        "add.s64 bd, %2, bs;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_base), "r"(b_step), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 struct UnitShape {
     int tA, n_kv;
     bool has_b;
