@@ -277,6 +277,7 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     AttnFwdArgs a = {};
     if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
     if ((rc = make_map(&a.tm_k, k, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_o, out, total_tokens, Hq, head_dim, 32)) != SPD_OK) return rc;
     if ((rc = make_map(&a.tm_v, v, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
     char *base = static_cast<char *>(ws);
     a.out = out;

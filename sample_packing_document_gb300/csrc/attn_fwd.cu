@@ -49,6 +49,7 @@ struct alignas(1024) FwdSmem {
     uint8_t q[2][D / 64][kAtom];
     uint8_t k[kStages][D / 64][kAtom];
     uint8_t v[kStages][D / 64][kAtom];
+    uint8_t ostage[8][32 * 128];   // per softmax warp: 32 rows x 64 d of O (bf16, 128-byte swizzle)
     uint64_t q_full, q_empty;
     uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
@@ -126,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tmem_relinquish();
     }
     if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&a.tm_o);
         tma_prefetch_desc(&a.tm_q);
         tma_prefetch_desc(&a.tm_k);
         tma_prefetch_desc(&a.tm_v);
@@ -387,33 +389,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 mbar_arrive(&sm.p_full[x]);
             }
             if (!ok) break;
-            // epilogue: normalise O_X and store it with the row's LSE
+            // epilogue: normalise O_X and store it with the row's LSE. O is read
+            // out of TMEM (as bf16) before anything is stored, so the next unit's
+            // first P V into O_X waits for the TMEM reads only.
             if (!warp_wait(&sm.o_done[x], o_cnt & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
             const int qi = d.y + tX * kTile + r;
             const bool valid = qi < d.z;
             const float inv_l = 1.f / l;
-            uint16_t *orow = a.out + (static_cast<size_t>(qi) * a.Hq + h) * D;
+            uint32_t ow[D / 2];   // O row as bf16 pairs
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + o_col + c * 32, o);
+            for (int c = 0; c < D / 32; c += 2) {
+                uint32_t o[2][32];
+                tmem_ld32(tmem + lane_off + o_col + c * 32, o[0]);
+                tmem_ld32(tmem + lane_off + o_col + c * 32 + 32, o[1]);
                 tmem_wait_ld();
-                uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+                for (int h2 = 0; h2 < 2; ++h2)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-                }
+                    for (int e = 0; e < 16; ++e)
+                        ow[(c + h2) * 16 + e] =
+                            pack_bf16x2(__uint_as_float(o[h2][2 * e]) * inv_l, __uint_as_float(o[h2][2 * e + 1]) * inv_l);
             }
-            if (valid) a.lse[static_cast<size_t>(h) * a.total_tokens + qi] = (m + log2f(l)) * 0.69314718055994531f;
             tc_fence_before();
             mbar_arrive(&sm.o_free[x]);
+            if (valid) a.lse[static_cast<size_t>(h) * a.total_tokens + qi] = (m + log2f(l)) * 0.69314718055994531f;
+            // A quarter wholly inside the segment leaves through TMA stores of
+            // [32 rows][64 d] boxes staged in this warp's slot (whole lines in HBM);
+            // a quarter reaching past the segment end is stored row by row (a box
+            // must not touch the next segment).
+            const int row0 = d.y + tX * kTile + (warp & 3) * 32;
+            if (row0 + 32 <= d.z) {
+                const uint32_t slot = smem_u32(sm.ostage[warp]);
+#pragma unroll
+                for (int half = 0; half < D / 64; ++half) {
+                    if (lane == 0) bulk_wait_group_read0();   // the slot's last store has been read
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(slot + lane * 128 + ((j ^ (lane & 7)) << 4), ow[half * 32 + 4 * j],
+                                     ow[half * 32 + 4 * j + 1], ow[half * 32 + 4 * j + 2], ow[half * 32 + 4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&a.tm_o, sm.ostage[warp], half * 64, h, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (valid) {
+                uint4 *dst = reinterpret_cast<uint4 *>(a.out + (static_cast<size_t>(qi) * a.Hq + h) * D);
+#pragma unroll
+                for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(ow[4 * e], ow[4 * e + 1], ow[4 * e + 2], ow[4 * e + 3]);
+            }
             ++o_cnt;
         }
+        if (lane == 0) bulk_wait_group0();   // this warp's O stores have landed
+        __syncwarp();
     }
 
     tc_fence_before();

@@ -96,6 +96,7 @@ size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs);
 // ---------------------------------------------------------------- attention
 struct AttnFwdArgs {
     CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_o;  // out as (d, Hq, T), boxes of 64 d x 32 rows
     uint16_t *out;
     float *lse;
     const Tile *tiles;
