@@ -86,6 +86,26 @@ enum {
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel);
 
 /*
+ * Failure-detection test hook. For the calling host thread, make the next
+ * spd_varlen_attn_fwd (which = SPD_DEBUG_SKIP_FWD_Q) or spd_varlen_attn_bwd
+ * (which = SPD_DEBUG_SKIP_BWD_KV) leave one producer arrive out: the TMA
+ * producer of each CTA does not load its first unit's Q tile pair (forward) or
+ * K / V tile (backward), so the consumer's bounded wait (2 s) runs out. The
+ * kernel then stops every role at its next bounded wait, lets its own copies
+ * land, frees its tensor memory and writes SPD_ERR_DEVICE_TIMEOUT into the
+ * status word; outputs are undefined, the CUDA context stays usable. The hook
+ * is consumed by that one call. SPD_DEBUG_SKIP_NONE clears it. Returns SPD_OK
+ * or SPD_ERR_INVALID_ARG. Not for production use; the pages have no
+ * counterpart.
+ */
+enum {
+    SPD_DEBUG_SKIP_NONE = 0,
+    SPD_DEBUG_SKIP_FWD_Q = 1,
+    SPD_DEBUG_SKIP_BWD_KV = 2
+};
+int spd_debug_skip_arrive(int which);
+
+/*
  * Synchronise `stream` and return the device status word of the last call
  * that used workspace `ws` (SPD_OK or a negative SPD_ERR_* code) in
  * *device_status (host). Returns SPD_OK or SPD_ERR_CUDA.

@@ -133,6 +133,21 @@ ProfileHook &profile_hook()
     return hook;
 }
 
+// The test hook of spd_debug_skip_arrive, per host thread.
+int &debug_skip_slot()
+{
+    static thread_local int which = SPD_DEBUG_SKIP_NONE;
+    return which;
+}
+
+int take_debug_skip(int which)
+{
+    int &s = debug_skip_slot();
+    if (s != which) return 0;
+    s = SPD_DEBUG_SKIP_NONE;
+    return 1;
+}
+
 }  // namespace spd
 
 using namespace spd;
@@ -156,6 +171,13 @@ const char *spd_status_string(int s)
 }
 
 int spd_version(void) { return 100; }
+
+int spd_debug_skip_arrive(int which)
+{
+    if (which < SPD_DEBUG_SKIP_NONE || which > SPD_DEBUG_SKIP_BWD_KV) return SPD_ERR_INVALID_ARG;
+    spd::debug_skip_slot() = which;
+    return SPD_OK;
+}
 
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel)
 {
@@ -291,6 +313,7 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.Hkv = Hkv;
     a.scale = softmax_scale;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.debug_skip = take_debug_skip(SPD_DEBUG_SKIP_FWD_Q);
     return cuda_rc(launch_attn_fwd(a, head_dim, (total_tokens + 2 * kTile - 1) / (2 * kTile) + num_segs, s));
 }
 
@@ -350,6 +373,7 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.Hkv = Hkv;
     a.scale = softmax_scale;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.debug_skip = take_debug_skip(SPD_DEBUG_SKIP_BWD_KV);
     return cuda_rc(launch_attn_bwd(a, head_dim, max_tiles(total_tokens, num_segs), s));
 }
 

@@ -169,11 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const int q0A = d.y + us.tA * kTile;
                 // Q_A, Q_B once the previous unit's last S MMA has read them
                 if (it > 0 && !mbar_wait(&sm.q_empty, (it - 1) & 1, abort_flag, a.status)) break;
-                mbar_arrive_expect_tx(&sm.q_full, (us.has_b ? 2 : 1) * kTileBytes);
-                for (int x = 0; x < (us.has_b ? 2 : 1); ++x)
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_3d(sm.q[x][c], &a.tm_q, c * 64, h, q0A + x * kTile, &sm.q_full);
-                ++q_loads;
+                if (!(a.debug_skip && it == 0)) {   // test hook: q_full of the first unit never completes
+                    mbar_arrive_expect_tx(&sm.q_full, (us.has_b ? 2 : 1) * kTileBytes);
+                    for (int x = 0; x < (us.has_b ? 2 : 1); ++x)
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_load_3d(sm.q[x][c], &a.tm_q, c * 64, h, q0A + x * kTile, &sm.q_full);
+                    ++q_loads;
+                }
                 bool ok = true;
                 for (int j = 0; j < us.n_kv; ++j, ++kv_iter) {
                     const int st = kv_iter % kStages, use = kv_iter / kStages;

@@ -19,6 +19,11 @@ struct ProfileHook {
 };
 ProfileHook &profile_hook();
 
+// Test hook of spd_debug_skip_arrive for the calling host thread: 1 if it is
+// armed for `which` (and then clears it), else 0.
+int &debug_skip_slot();
+int take_debug_skip(int which);
+
 inline void prof_begin(int which, cudaStream_t s)
 {
     ProfileHook &h = profile_hook();
@@ -108,6 +113,7 @@ struct AttnFwdArgs {
     int32_t grid_tiles;  // tile slots per head in the grid (blockIdx = head * grid_tiles + tile)
     float scale_log2;    // softmax_scale * log2(e)
     float scale;
+    int debug_skip;      // test hook: the producer leaves its first Q load out
 };
 
 cudaError_t launch_attn_fwd(const AttnFwdArgs &a, int head_dim, int64_t grid_tiles,
@@ -133,6 +139,7 @@ struct AttnBwdArgs {
     int32_t Hq, Hkv;
     float scale_log2;
     float scale;
+    int debug_skip;      // test hook: the producer leaves its first K / V load out
 };
 
 cudaError_t launch_attn_bwd(const AttnBwdArgs &a, int head_dim, int64_t max_units,

@@ -26,6 +26,7 @@ SIGNATURES = {
     "spd_version": (_INT, []),
     "spd_read_status": (_INT, [_P, _P, ctypes.POINTER(_INT)]),
     "spd_set_profile_events": (_INT, [_P, _P, _INT]),
+    "spd_debug_skip_arrive": (_INT, [_INT]),
     "spd_pack_rows": (_INT, [_I64, _I64, _INT, _INT, _INT, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "spd_pack_workspace_size": (_SZ, [_I64]),
     "spd_pack_tokens": (_INT, [_P, _P, _I64, _I64, _INT, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -107,6 +108,16 @@ def set_profile_events(begin, end, kernel):
     b = ctypes.c_void_p(begin.cuda_event) if begin is not None else None
     e = ctypes.c_void_p(end.cuda_event) if end is not None else None
     _check("spd_set_profile_events", load().spd_set_profile_events(b, e, int(kernel)))
+
+
+DEBUG_SKIP_NONE, DEBUG_SKIP_FWD_Q, DEBUG_SKIP_BWD_KV = 0, 1, 2
+
+
+def debug_skip_arrive(which):
+    """Failure-detection test hook (see spd_debug_skip_arrive): the next
+    forward (DEBUG_SKIP_FWD_Q) or backward (DEBUG_SKIP_BWD_KV) call on this
+    thread leaves one producer arrive out and reports a device timeout."""
+    _check("spd_debug_skip_arrive", load().spd_debug_skip_arrive(int(which)))
 
 
 # ----------------------------------------------------------------------------- packing

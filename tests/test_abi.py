@@ -81,3 +81,14 @@ def test_oracle_does_not_leak_into_product():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", text, re.M), f
                 assert "oracle/" not in text and "liboracle" not in text, f
+
+
+def test_debug_skip_hook_validates_its_argument():
+    """The failure-detection test hook accepts only its three codes (host only)."""
+    from sample_packing_document_gb300 import build, ops
+    build.build()
+    lib = ops.load()
+    assert lib.spd_debug_skip_arrive(3) == -1
+    assert lib.spd_debug_skip_arrive(-1) == -1
+    assert lib.spd_debug_skip_arrive(ops.DEBUG_SKIP_FWD_Q) == 0
+    assert lib.spd_debug_skip_arrive(ops.DEBUG_SKIP_NONE) == 0   # cleared again
