@@ -23,19 +23,20 @@
 //                                            TMA reduce-add into the HBM accumulator.
 //   bwd_dq_kernel    dq = scale * accumulator, in the output layout and type.
 //
-// Warp roles (576 threads). Warp w works on TMEM lanes 32 (w % 4) .. +31 (kv
-// rows; q rows for the dQ read-out) and on one half of the columns:
-//   warps 0-7   "P": P^T(i) = exp(S^T(i) * scale - LSE) from region A, written
-//               back into it as bf16 (the P^T columns of a half sit in the first
-//               half of that half's S^T columns); then one 32 x 32 chunk of the
-//               dQ(i) read-out, staged in the spent Q(i) stage, and its reduce-add.
-//   warps 8-15  "dS": dS^T(i) = P^T(i) (dP^T(i) - D) into shared memory, then one
-//               chunk of the dQ(i) read-out, staged in the dS buffer; at the end
-//               the dK / dV stores.
+// Warp roles (640 threads: four compute warpgroups, and one for the TMA
+// producer, the MMA issuer and two idle warps). Compute warp w works on TMEM
+// lanes 32 (w % 4) .. +31 (kv rows; q rows for the dQ read-out):
+//   warps 0-7   "P": P^T(i) = exp(S^T(i) * scale - LSE) on one half of the
+//               columns of region A, written back into it as bf16 (the P^T
+//               columns of a half sit in the first half of that half's S^T
+//               columns). Nothing else, so P(i+1) starts as soon as S^T(i+1) is
+//               in.
+//   warps 8-15  "dS": dS^T(i) = P^T(i) (dP^T(i) - D) into shared memory, then the
+//               dQ(i) read-out (two 32 x 32 chunks per warp for d = 128, staged
+//               in the spent Q(i) stage and in the dS buffer and added by the TMA
+//               engine); at the end of a unit the dV and dK stores.
 //   warp 16     TMA producer; warp 17 issues the MMAs in the order
-//              dV(i), dK(i), dQ(i), S(i+1), dP(i+1), dV(i+1), ...
-// so P(i+1) is computed while dK(i) / dQ(i) run, dS(i) while dV(i) runs, and the
-// dQ(i) read-out while S(i+1) runs.
+//               dV(i), dK(i), dQ(i), S(i+1), dP(i+1), dV(i+1), ...
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -66,6 +67,7 @@ struct BwdSmem {
     uint64_t kv_full, kv_empty;
     uint64_t q_full[kQStages], q_empty[kQStages], do_full[kQStages], do_empty[kQStages];
     uint64_t s_full, dp_full, p_full, ds_full, dq_full, dq_free;
+    uint64_t acc_full, acc_free;     // unit's MMAs complete / its dV, dK read out
     uint64_t cols_l[2], cols_d[2];   // the step's lse2 / delta written
     uint64_t unit_full[2], unit_empty[2];
     int4 unit[2];                    // work unit in flight: {kv head (-1: no more work), seg_start, seg_end, kv tile}
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(&sm.kv_empty, 1);
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(&sm.q_full[s], 1);
-            mbar_init(&sm.q_empty[s], 4 * (D / 64));  // the P warps that stage dQ there, once it is read
+            mbar_init(&sm.q_empty[s], kDsWarps);   // the dS warps, once their staged dQ chunks have been read
             mbar_init(&sm.do_full[s], 1);
             mbar_init(&sm.do_empty[s], 1);
         }
@@ -272,7 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         mbar_init(&sm.p_full, 32 * kPWarps);
         mbar_init(&sm.ds_full, 32 * kDsWarps);
         mbar_init(&sm.dq_full, 1);
-        mbar_init(&sm.dq_free, 32 * (kPWarps + kDsWarps));
+        mbar_init(&sm.dq_free, 32 * kDsWarps);
+        mbar_init(&sm.acc_full, 1);
+        mbar_init(&sm.acc_free, kDsWarps);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.cols_l[b], 128);
             mbar_init(&sm.cols_d[b], 128);
@@ -445,8 +449,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     const int st = gi % kQStages;
                     const uint32_t ph = gi & 1;
                     // dV += P^T dO: P^T in TMEM over S^T (M = kv, K = q), dO MN-major.
-                    // The first step of a unit overwrites the dV the P warps have read out.
+                    // The first step of a unit overwrites dV (accumulate = 0).
                     if (!mbar_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
+                    // the first dV of a unit overwrites the last unit's dV: read out by then
+                    if (i == 0 && it > 0 && !mbar_wait(&sm.acc_free, (it - 1) & 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
                     {
                         const uint64_t dod = sdesc_sw128(smem_u32(sm.dout[st][0]), kAtom, 1024);
@@ -479,6 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 }
                 if (!ok) break;
                 umma_commit(&sm.kv_empty);   // K / V fully read: the next unit's may load
+                umma_commit(&sm.acc_full);   // dV / dK of the unit final
                 ++kv_commits;
             }
             umma_commit(&sm.drain);
@@ -502,9 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         const float sl2 = a.scale_log2;
         const uint32_t ds_addr = smem_u32(sm.ds[0]);
         const bool loader = half == 0;                            // loads the step's LSE / D column t
-        // dQ read-out chunk (d columns 32 c ..): P warps take the first D / 64, dS warps the rest
-        const int my_chunk = is_p ? half : D / 64 + half;
-        const bool reads_out = is_p ? my_chunk < D / 64 : my_chunk < D / 32;
         auto col_term = [&](const int4 &u, int i) -> float {
             const int nq = seg_tiles(u) - u.w;
             const int h = u.x * group + i / nq;
@@ -513,13 +520,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             const size_t x = static_cast<size_t>(h) * a.total_tokens + qi;
             return is_p ? a.lse[x] * 1.4426950408889634f : a.delta[x];
         };
-        // Stages one [32 rows][32 cols] chunk of dQ (TMEM region B) in the 128-byte-
-        // swizzled layout and lets the TMA engine add it into the accumulator in
-        // the background. Rows past the segment carry exact zeros.
-        auto dq_readout = [&](const uint8_t *stage, int q0, int seg_end, int h) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + kB + my_chunk * 32, v);
-            tmem_wait_ld();
+        // dS warps' staging slots: A in the step's spent Q stage (d = 128), B in
+        // the dS buffer (free once dK / dQ, its readers, have completed).
+        auto slot_a = [&](int gs) -> uint8_t * {
+            return D == 128 ? sm.q[gs % kQStages][0] + (quarter + 4 * half) * 4096
+                            : sm.ds[0] + (quarter + 4 * half) * 4096;
+        };
+        uint8_t *const slot_b = sm.ds[0] + (quarter + 4 * half) * 4096;
+        // Stages one [32 rows][32 cols] chunk of dQ (registers v, d columns
+        // 32 chunk ..) in the 128-byte-swizzled layout and lets the TMA engine add
+        // it into the accumulator in the background. Rows past the segment carry
+        // exact zeros.
+        auto dq_stage = [&](const uint32_t (&v)[32], uint8_t *stage, int chunk, int q0, int seg_end, int h) {
             const uint32_t stage_addr = smem_u32(stage);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -529,13 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) {
                 if (q0 + quarter * 32 < seg_end)   // skip a chunk of padding rows only
-                    tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, h * (D / 32) + my_chunk);
+                    tma_reduce_add_3d(&a.tm_dqacc, stage, 0, q0 + quarter * 32, h * (D / 32) + chunk);
                 bulk_commit_group();
             }
-        };
-        auto store_rows = [&](const int4 &u, int gs_last) {
-            const uint8_t *slot = (is_p ? sm.q[gs_last % kQStages][0] : sm.ds[0]) + (quarter + 4 * half) * 4096;
-            store_acc_rows<D, is_p>(a, tmem + lane_off + (is_p ? kC : kE) + half * (D / 2), u, quarter, half, slot);
         };
 
         int4 cur;
@@ -558,10 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     if (i + 1 < nsteps) nxt = col_term(cur, i + 1);
                 }
                 if (!warp_wait(colbar, (gi >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-                const float *CC = colbuf + col0;
+                const float4 *CC = reinterpret_cast<const float4 *>(colbuf + col0);
                 if constexpr (is_p) {
                     // P^T = exp(S^T * scale - LSE); column col0 + c (q row q0 + col0 + c)
-                    // is live for kv row kj iff kj <= q row < seg_end
+                    // is live for kv row kj iff kj <= q row < seg_end. The P warps do
+                    // nothing else, so P of the next step starts as soon as its S^T is in.
                     const int c_lo = kj - q0 - col0, c_hi = cur.z - q0 - col0;
                     const bool full = c_lo <= 0 && c_hi >= 64;
                     if (!warp_wait(&sm.s_full, ph, abort_flag, a.status)) { ok = false; break; }
@@ -575,41 +584,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                         tmem_wait_ld();
                         uint32_t pk[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int col = c * 32 + 2 * e;
-                            float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - CC[col]);
-                            float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - CC[col + 1]);
-                            if (!full) {
-                                if (col < c_lo || col >= c_hi) p0 = 0.f;
-                                if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 l4 = CC[c * 8 + e4];   // one broadcast load for four columns
+                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const int e = e4 * 2 + e2, col = c * 32 + 2 * e;
+                                float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - lv[2 * e2]);
+                                float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - lv[2 * e2 + 1]);
+                                if (!full) {
+                                    if (col < c_lo || col >= c_hi) p0 = 0.f;
+                                    if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
+                                }
+                                pk[e] = pack_bf16x2(p0, p1);
                             }
-                            pk[e] = pack_bf16x2(p0, p1);
                         }
                         tmem_st16(tmem + lane_off + kA + col0 + c * 16, pk);
                     }
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive(&sm.p_full);
-                    // The previous Q stage held this warp's staged dQ chunk: once the TMA
-                    // engine has read it (it had the whole P computation to do so) the
-                    // stage goes back to the producer.
-                    if (gi > 0 && reads_out) {
-                        if (lane == 0) {
-                            bulk_wait_group_read0();
-                            mbar_arrive(&sm.q_empty[(gi - 1) % kQStages]);
-                        }
-                        __syncwarp();
-                    }
                 } else {
                     // dS^T = P^T * (dP^T - D); P^T read back from TMEM (bf16), masked entries are 0
                     if (!warp_wait(&sm.dp_full, ph, abort_flag, a.status)) { ok = false; break; }
                     if (!warp_wait(&sm.p_full, ph, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
-                    // This warp's slice of the dS buffer held its staged dQ chunk of the
-                    // previous step: reusable once the TMA engine has read it (the dK /
-                    // dQ MMAs, its other readers, completed before that step's dq_full).
-                    if (gi > 0 && reads_out) {
-                        if (lane == 0) bulk_wait_group_read0();
+                    // This warp's staged chunks of the previous step (the dS buffer one and
+                    // the Q stage one) must have been read by the TMA engine before dS is
+                    // written over the former; the Q stage then goes back to the producer.
+                    if (gi > 0) {
+                        if (lane == 0) {
+                            bulk_wait_group_read0();
+                            mbar_arrive(&sm.q_empty[(gi - 1) % kQStages]);
+                        }
                         __syncwarp();
                     }
 #pragma unroll
@@ -620,11 +627,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                         tmem_wait_ld();
                         uint32_t pk[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int col = c * 32 + 2 * e;
-                            const float d0 = bf16_lo(pv[e]) * (__uint_as_float(dp[2 * e]) - CC[col]);
-                            const float d1 = bf16_hi(pv[e]) * (__uint_as_float(dp[2 * e + 1]) - CC[col + 1]);
-                            pk[e] = pack_bf16x2(d0, d1);
+                        for (int e4 = 0; e4 < 8; ++e4) {
+                            const float4 d4 = CC[c * 8 + e4];
+                            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const int e = e4 * 2 + e2;
+                                const float d0 = bf16_lo(pv[e]) * (__uint_as_float(dp[2 * e]) - dv4[2 * e2]);
+                                const float d1 = bf16_hi(pv[e]) * (__uint_as_float(dp[2 * e + 1]) - dv4[2 * e2 + 1]);
+                                pk[e] = pack_bf16x2(d0, d1);
+                            }
                         }
                         // row t, q columns col0 + 32c .. +31: atom `half`, 16-byte chunks 4c .. 4c+3
 #pragma unroll
@@ -637,32 +649,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     fence_proxy_async_smem();
                     tc_fence_before();
                     mbar_arrive(&sm.ds_full);
+                    // dQ read-out: this warp's rows of d columns 32 half (and 32 (half + 2)
+                    // for d = 128). Both TMEM loads land before B is released for the next
+                    // dP^T; the chunks are then staged and added in the background.
+                    if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t va[32], vb[32];
+                    tmem_ld32(tmem + lane_off + kB + half * 32, va);
+                    if (D == 128) tmem_ld32(tmem + lane_off + kB + (half + 2) * 32, vb);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(&sm.dq_free);
+                    dq_stage(va, slot_a(gi), half, q0, cur.z, h);
+                    if (D == 128) dq_stage(vb, slot_b, half + 2, q0, cur.z, h);
                 }
-                // dQ read-out of one chunk, staged in this warp's slice of the spent
-                // Q stage (P warps: Q was last read by dK, complete at dq_full) or of
-                // the dS buffer (dS warps: dK / dQ, its readers, complete at dq_full).
-                if (!warp_wait(&sm.dq_full, ph, abort_flag, a.status)) { ok = false; break; }
-                tc_fence_after();
-                if (reads_out) {
-                    const uint8_t *stage = is_p ? sm.q[gi % kQStages][0] + (quarter + 4 * my_chunk) * 4096
-                                                : sm.ds[0] + (quarter + 4 * half) * 4096;
-                    dq_readout(stage, q0, cur.z, h);
-                }
-                tc_fence_before();
-                mbar_arrive(&sm.dq_free);
             }
             if (!ok) break;
-            // Every MMA of the unit has completed (its last dq_full). Take the next
-            // unit and start its first column load, then read out this unit's dV / dK;
-            // the next unit's first dV / dK MMAs wait for p_full / ds_full, which
-            // these warps signal only after the read-out.
+            // Take the next unit and start its first column load. The dS warps then
+            // read out this unit's dV and dK once all its MMAs have completed
+            // (acc_full) and release the accumulators (acc_free) before the next
+            // unit's first dV MMA; the P warps go straight on.
             int4 nu;
             if (!warp_unit(it + 1, nu)) { ok = false; break; }
             if (loader && nu.x >= 0) nxt = col_term(nu, 0);
-            store_rows(cur, gi - 1);
+            if constexpr (!is_p) {
+                if (!warp_wait(&sm.acc_full, it & 1, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                store_acc_rows<D, true>(a, tmem + lane_off + kC + half * (D / 2), cur, quarter, half, slot_a(gi - 1));
+                store_acc_rows<D, false>(a, tmem + lane_off + kE + half * (D / 2), cur, quarter, half, slot_b);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.acc_free);
+            }
             cur = nu;
         }
-        if (lane == 0) bulk_wait_group0();     // every reduce of this warp has landed
+        if (lane == 0) bulk_wait_group0();     // every reduce / store of this warp has landed
         __syncwarp();
         };
         if (warp < kPWarps) compute(std::true_type{});
