@@ -46,10 +46,12 @@ namespace spd {
 namespace {
 
 constexpr int kThreads = 640;        // 16 compute warps (4 warpgroups) + producer + MMA issuer + 2 idle warps
-// Register split (setmaxnreg): the launch gives 96 per thread (640 x 96 = 61440); the
-// warpgroup of the producer / MMA issuer drops to 64 and the four compute
-// warpgroups rise to 104: 4 x 128 x 104 + 128 x 64 = 61440.
-constexpr uint32_t kComputeRegs = 104, kControlRegs = 64;
+// Register split (setmaxnreg, per warpgroup): the launch gives 96 per thread
+// (640 x 96 = 61440); the warpgroup of the producer / MMA issuer drops to 48, the
+// two P warpgroups rise to 112 and the two dS warpgroups to 104:
+// 2 x 128 x 112 + 2 x 128 x 104 + 128 x 48 = 61440. Per SM sub-partition (one
+// warp of each warpgroup): (112 + 112 + 104 + 104 + 48) x 32 = 15360 <= 16384.
+constexpr uint32_t kPRegs = 112, kDsRegs = 104, kControlRegs = 48;
 constexpr int kPWarps = 8, kDsWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;
@@ -499,7 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         }
     }
     } else {
-        setmaxnreg_inc<kComputeRegs>();
         // ------------------------------------------------------------ compute warps
         // One body, instantiated for the P warps and for the dS warps.
         auto compute = [&](auto role) {
@@ -575,13 +576,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     const bool full = c_lo <= 0 && c_hi >= 64;
                     if (!warp_wait(&sm.s_full, ph, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
-                    // P^T columns col0 + 32c .. +31 (bf16 pairs) go to TMEM columns col0 + 16c ..
-                    // +15, inside the S^T columns this warp has already read itself.
+                    // Both S^T chunks are read before P^T is written: P^T columns col0 + 32c ..
+                    // +31 (bf16 pairs) go to TMEM columns col0 + 16c .. +15.
+                    uint32_t sv2[2][32];
+                    tmem_ld32(tmem + lane_off + kA + col0, sv2[0]);
+                    tmem_ld32(tmem + lane_off + kA + col0 + 32, sv2[1]);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        uint32_t sv[32];
-                        tmem_ld32(tmem + lane_off + kA + col0 + c * 32, sv);
-                        tmem_wait_ld();
+                        const uint32_t (&sv)[32] = sv2[c];
                         uint32_t pk[16];
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
@@ -686,8 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         if (lane == 0) bulk_wait_group0();     // every reduce / store of this warp has landed
         __syncwarp();
         };
-        if (warp < kPWarps) compute(std::true_type{});
-        else compute(std::false_type{});
+        if (warp < kPWarps) {
+            setmaxnreg_inc<kPRegs>();
+            compute(std::true_type{});
+        } else {
+            setmaxnreg_inc<kDsRegs>();
+            compute(std::false_type{});
+        }
     }
 
     tc_fence_before();
