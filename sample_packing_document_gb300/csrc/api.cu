@@ -294,7 +294,7 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     if (rc != SPD_OK) return rc;
     if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
 
-    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, 2, ws, s));
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, 2, sms, ws, s));
     if (rc != SPD_OK) return rc;
     AttnFwdArgs a = {};
     if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
@@ -307,6 +307,7 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
     a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
     a.work_counter = reinterpret_cast<int32_t *>(base) + 2;
+    a.long_count = reinterpret_cast<const int32_t *>(base) + 3;
     a.status = reinterpret_cast<int *>(base);
     a.total_tokens = static_cast<int32_t>(total_tokens);
     a.Hq = Hq;
@@ -341,7 +342,7 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     if (rc != SPD_OK) return rc;
     if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
 
-    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 1, 1, ws, s));
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 1, 1, sms, ws, s));
     if (rc != SPD_OK) return rc;
     AttnBwdArgs a = {};
     if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
@@ -367,6 +368,7 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
     a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
     a.work_counter = reinterpret_cast<int32_t *>(base) + 2;
+    a.long_count = reinterpret_cast<const int32_t *>(base) + 3;
     a.status = reinterpret_cast<int *>(base);
     a.total_tokens = static_cast<int32_t>(total_tokens);
     a.Hq = Hq;

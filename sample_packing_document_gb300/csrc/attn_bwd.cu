@@ -327,14 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     if (warp == 16) {
         // ------------------------------------------------------------ producer
         // Takes work units (kv head, kv tile) from the shared counter in list
-        // order: kv-head-major, so the CTAs of one kv head run together and the
-        // Q / dO tiles they share and the dQ rows they add into stay in L2;
-        // longest first inside a head. Q / dO stream through a 2-stage ring that
+        // order (unit_of): the few units much longer than a kv head's share of an
+        // SM first, across kv heads; then kv-head-major, so the CTAs of one kv
+        // head run together and the Q / dO tiles they share and the dQ rows they
+        // add into stay in L2; longest first inside a head. Q / dO stream through a 2-stage ring that
         // runs on across units; the next unit's K / V are pulled into L2 as soon
         // as it is taken and copied in once the last MMA reading K has completed.
         if (lane == 0) {
             const int n_tiles = *a.tile_count;
             const int total_units = n_tiles * a.Hkv;
+            const int n_long = *a.long_count;
             int gi = 0, kv_loads = 0;
             int last_q[kQStages], last_do[kQStages];
             for (int s = 0; s < kQStages; ++s) last_q[s] = last_do[s] = -1;
@@ -360,8 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 const int w = *abort_flag ? total_units : atomicAdd(a.work_counter, 1);
                 int4 d = make_int4(-1, 0, 0, 0);
                 if (w < total_units) {
-                    const Tile tl = a.tiles[w % n_tiles];
-                    d = make_int4(w / n_tiles, tl.seg_start, tl.seg_end, tl.t);
+                    int head, idx;
+                    unit_of(w, n_tiles, n_long, a.Hkv, head, idx);
+                    const Tile tl = a.tiles[idx];
+                    d = make_int4(head, tl.seg_start, tl.seg_end, tl.t);
                 }
                 sm.unit[slot] = d;
                 mbar_arrive(&sm.unit_full[slot]);

@@ -140,14 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     constexpr uint32_t kTileBytes = 128 * D * 2;
     const int units_per_head = *a.tile_count;
     const int total_units = units_per_head * a.Hq;
+    const int n_long = *a.long_count;
 
     if (warp >= 8) {
     setmaxnreg_dec<kControlRegs>();
     if (warp == 8) {
         // ------------------------------------------------------------ producer
-        // Takes work units from the shared counter in list order: head-major
-        // (the CTAs on one head run together, so the K / V tiles they share stay
-        // in L2), longest first inside a head.
+        // Takes work units from the shared counter in list order (unit_of): the
+        // few units much longer than a head's share of an SM first, across heads;
+        // then head-major (the CTAs on one head run together, so the K / V tiles
+        // they share stay in L2), longest first inside a head.
         if (lane == 0) {
             uint32_t kv_iter = 0;
             int last_kv_use[kStages] = {-1, -1};
@@ -158,8 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const int u = *abort_flag ? total_units : atomicAdd(a.work_counter, 1);
                 int4 d = make_int4(-1, 0, 0, 0);
                 if (u < total_units) {
-                    const Tile tl = a.tiles[u % units_per_head];
-                    d = make_int4(u / units_per_head, tl.seg_start, tl.seg_end, tl.t);
+                    int head, idx;
+                    unit_of(u, units_per_head, n_long, a.Hq, head, idx);
+                    const Tile tl = a.tiles[idx];
+                    d = make_int4(head, tl.seg_start, tl.seg_end, tl.t);
                 }
                 sm.unit[slot] = d;
                 mbar_arrive(&sm.unit_full[slot]);

@@ -36,6 +36,8 @@ inline void prof_end(int which, cudaStream_t s)
 }
 
 // Workspace header: [0] status word, [1] tile count; the rest per operation.
+// Workspace header (int32 words): [0] status, [1] work units per head, [2] work
+// counter of the persistent kernels, [3] long units per head (see unit_of).
 constexpr size_t kWsHeader = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -94,8 +96,26 @@ inline int64_t max_tiles(int64_t total_tokens, int64_t num_segs)
 // to ws[1]. order: 0 = forward costs, 1 = backward costs (n - t). unit: tiles
 // per work unit (2 = a pair of consecutive q tiles, forward only); Tile.t is
 // the unit's first tile.
+// Work unit w of `heads` x n_tiles, the tile list of every head sorted by cost
+// (largest first): the first n_long tiles of every head (the units much longer
+// than a head's share of one SM) come first, interleaved across heads so the
+// longest start first; then the rest, head-major (the CTAs on one head run
+// together, so the tiles they share stay in L2).
+__device__ __forceinline__ void unit_of(int w, int n_tiles, int n_long, int heads, int &head, int &idx)
+{
+    const int lead = n_long * heads;
+    if (w < lead) {
+        head = w % heads;
+        idx = w / heads;
+    } else {
+        const int r = w - lead, per = n_tiles - n_long;
+        head = r / per;
+        idx = n_long + r % per;
+    }
+}
+
 cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
-                            int order, int unit, void *ws, cudaStream_t stream);
+                            int order, int unit, int num_sms, void *ws, cudaStream_t stream);
 size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs);
 
 // ---------------------------------------------------------------- attention
@@ -107,6 +127,7 @@ struct AttnFwdArgs {
     const Tile *tiles;
     const int32_t *tile_count;
     int32_t *work_counter;  // next work unit (zeroed by the scheduler kernel)
+    const int32_t *long_count;  // long units per head (see unit_of)
     int *status;
     int32_t total_tokens;
     int32_t Hq, Hkv;
@@ -134,6 +155,7 @@ struct AttnBwdArgs {
     const Tile *tiles;
     const int32_t *tile_count;
     int32_t *work_counter;  // next work unit (zeroed by the scheduler kernel)
+    const int32_t *long_count;  // long units per head (see unit_of)
     int *status;
     int32_t total_tokens;
     int32_t Hq, Hkv;

@@ -51,18 +51,21 @@ __device__ long long block_scan_excl(long long v, long long *total, long long *s
 }
 
 __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, int32_t nsegs,
-                                                            int64_t T, int order, int unit, int *status,
-                                                            int32_t *count, Tile *tiles,
+                                                            int64_t T, int order, int unit, int num_sms,
+                                                            int *status, int32_t *count, Tile *tiles,
                                                             int32_t *tile_off)
 {
     __shared__ int bins[kCostCap + 1];
     __shared__ long long sh[33];
     __shared__ int bad_s;
+    __shared__ unsigned long long total_cost;
     const int tid = threadIdx.x;
     if (tid == 0) {
         *status = 0;
         count[1] = 0;   // work counter of the persistent kernels
+        count[2] = 0;   // long units per head
         bad_s = 0;
+        total_cost = 0;
     }
     for (int c = tid; c <= kCostCap; c += kThreads) bins[c] = 0;
     __syncthreads();
@@ -109,12 +112,25 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
         else cost = (t + 1) + (unit > 1 && t + 1 < n ? t + 2 : 0);  // forward: kv tiles of each q tile
     };
 
+    unsigned long long my_cost = 0;
     for (int i = tid; i < ntiles; i += kThreads) {
         int s, t, n, cost;
         locate(i, s, t, n, cost);
         atomicAdd(&bins[min(cost, kCostCap)], 1);
+        my_cost += static_cast<unsigned long long>(cost);
     }
+    atomicAdd(&total_cost, my_cost);
     __syncthreads();
+    // Long units: cost at least twice one SM's share of a head's total. They are
+    // taken first, across heads (see unit_of), so none starts late in the list.
+    // (Costs above kCostCap share a bin and are not told apart: then none is long.)
+    {
+        const long long c_long = max(4LL, (2LL * static_cast<long long>(total_cost) + num_sms - 1) / num_sms);
+        int n_long = 0;
+        if (c_long <= kCostCap)
+            for (int c = static_cast<int>(c_long) + tid; c <= kCostCap; c += kThreads) n_long += bins[c];
+        if (n_long) atomicAdd(&count[2], n_long);
+    }
     // Descending exclusive scan: bins[c] <- number of tiles with a larger cost.
     // Thread tid owns costs kCostCap - 4 tid .. kCostCap - 4 tid - 3.
     {
@@ -156,7 +172,7 @@ size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs)
 }
 
 cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
-                            int order, int unit, void *ws, cudaStream_t stream)
+                            int order, int unit, int num_sms, void *ws, cudaStream_t stream)
 {
     char *base = reinterpret_cast<char *>(ws);
     int *status = reinterpret_cast<int *>(base);
@@ -164,8 +180,8 @@ cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t
     Tile *tiles = reinterpret_cast<Tile *>(base + kWsHeader);
     int32_t *tile_off = reinterpret_cast<int32_t *>(
         base + kWsHeader + align_up(sizeof(Tile) * static_cast<size_t>(max_tiles(total_tokens, num_segs)), 256));
-    schedule_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_segs, total_tokens, order, unit, status,
-                                                count, tiles, tile_off);
+    schedule_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_segs, total_tokens, order, unit,
+                                                num_sms > 0 ? num_sms : 1, status, count, tiles, tile_off);
     return cudaGetLastError();
 }
 
