@@ -168,6 +168,12 @@ def dist_barrier(ws):
         dist.barrier()
 
 
+def replica_value(ws, flops_per_rank, ms_max):
+    """Whole-job TFLOP/s of ws independent replicas: every rank does
+    flops_per_rank per step, the job's step time is the slowest rank's."""
+    return ws * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample(w, seg_lens, cu, budget_pairs):
@@ -390,7 +396,7 @@ def main():
     ms = dist_max(ms_local, ws_n)
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["fwd"])
     bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["bwd"])
-    value = ws_n * fl["total"] / (ms * 1e-3) / 1e12
+    value = replica_value(ws_n, fl["total"], ms)
 
     pk_, how = peaks()
     peak = pk_.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
