@@ -331,9 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const bool diag = (j == tX);
                 // The whole S row (128 columns) is read once into registers.
                 uint32_t sv[128];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    tmem_ld32(tmem + lane_off + s_col + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+                tmem_ld128(tmem + lane_off + s_col, sv);
                 tmem_wait_ld();
                 // row max, 8 independent chains
                 float mxs[8];
