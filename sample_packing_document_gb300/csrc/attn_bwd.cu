@@ -583,8 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                     // Both S^T chunks are read before P^T is written: P^T columns col0 + 32c ..
                     // +31 (bf16 pairs) go to TMEM columns col0 + 16c .. +15.
                     uint32_t sv2[2][32];
-                    tmem_ld32(tmem + lane_off + kA + col0, sv2[0]);
-                    tmem_ld32(tmem + lane_off + kA + col0 + 32, sv2[1]);
+                    tmem_ld64(tmem + lane_off + kA + col0, *reinterpret_cast<uint32_t(*)[64]>(&sv2[0][0]));
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
