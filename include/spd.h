@@ -17,6 +17,10 @@
  *                        one causal attention per document).
  *   spd_varlen_attn_bwd  its exact gradient (dQ, dK, dV).
  *
+ * and the data steps that follow packing (page "Data loading and flow",
+ * section "Processing data"): spd_unpack_data and
+ * spd_split_sequence_parallel.
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Pointers are DEVICE pointers unless the argument says "host". The caller
@@ -81,7 +85,9 @@ enum {
     SPD_PROFILE_NONE = 0,
     SPD_PROFILE_PACK_STREAM = 1,
     SPD_PROFILE_ATTN_FWD = 2,
-    SPD_PROFILE_ATTN_BWD = 3
+    SPD_PROFILE_ATTN_BWD = 3,
+    SPD_PROFILE_UNPACK = 4,   /* the kernel of spd_unpack_data */
+    SPD_PROFILE_SPLIT = 5     /* the kernel of spd_split_sequence_parallel */
 };
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel);
 
@@ -172,6 +178,46 @@ int spd_pack_tokens(const int32_t *tokens, const int32_t *doc_lens, int64_t num_
                     int32_t *input_ids, int32_t *labels, int32_t *indexes, int32_t *cu_seqlens,
                     int32_t *row_seg_ptr, int32_t *max_seqlen, int32_t *num_segs, void *ws,
                     size_t ws_bytes, spd_stream_t stream);
+
+/*
+ * unpack_data (page "Data loading and flow", section "Processing data", the
+ * use_packed_dataset=False path): every packed row holds at most micro_bsz
+ * documents as segments; segment m of row r becomes output row (r, m) of
+ * seq_len positions, its first min(length, seq_len) tokens copied from
+ * input_ids / labels and the rest 0 / -100. Output rows without a segment are
+ * all 0 / -100; segments beyond the first micro_bsz of a row (none in rows that
+ * spd_pack_tokens built with use_packed_dataset == 0) are dropped. cu_seqlens
+ * and indexes have no unpacked form (the page drops them).
+ *
+ * Inputs (device), as spd_pack_tokens writes them: input_ids, labels int32
+ *   [rows * micro_bsz * seq_len]; cu_seqlens int32 (global offsets);
+ *   row_seg_ptr int32 [rows + 1].
+ * Outputs (device): out_ids, out_labels int32 [rows][micro_bsz][seq_len].
+ * rows == 0 is a no-op. Returns SPD_ERR_INVALID_ARG (micro_bsz or seq_len < 1,
+ * rows < 0, rows * micro_bsz * seq_len > 2^31 - 1, a null or unaligned
+ * pointer), SPD_ERR_UNSUPPORTED (not an sm_103 GPU) or SPD_ERR_CUDA. No
+ * workspace: the segment offsets are trusted as spd_pack_tokens produced them.
+ */
+int spd_unpack_data(const int32_t *input_ids, const int32_t *labels, const int32_t *cu_seqlens,
+                    const int32_t *row_seg_ptr, int64_t rows, int micro_bsz, int seq_len, int32_t *out_ids,
+                    int32_t *out_labels, spd_stream_t stream);
+
+/*
+ * split_data_sequence_parallel (page "Data loading and flow", section
+ * "Processing data", isp with tp size > 1): rank `rank` of sp_size keeps the
+ * contiguous chunk [rank * len / sp_size, (rank + 1) * len / sp_size) of the
+ * sequence dimension of every row. Up to three int32 tensors of one shape
+ * [rows][len] per call (the page splits input_ids, indexes and labels; an
+ * unpacked batch has no indexes): src_i -> dst_i int32 [rows][len / sp_size];
+ * unused slots are NULL (src_i and dst_i together). Returns
+ * SPD_ERR_INVALID_ARG if len % sp_size != 0 (the sequence must be padded
+ * first), sp_size < 1, rank outside [0, sp_size), rows < 0, len < 0,
+ * rows * len > 2^31 - 1, or a pointer is unaligned / unpaired;
+ * SPD_ERR_UNSUPPORTED or SPD_ERR_CUDA as above.
+ */
+int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const int32_t *src2, int64_t rows,
+                                int64_t len, int sp_size, int rank, int32_t *dst0, int32_t *dst1, int32_t *dst2,
+                                spd_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Attention                                                                 */

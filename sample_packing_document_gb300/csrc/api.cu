@@ -181,7 +181,7 @@ int spd_debug_skip_arrive(int which)
 
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel)
 {
-    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_ATTN_BWD) return SPD_ERR_INVALID_ARG;
+    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_SPLIT) return SPD_ERR_INVALID_ARG;
     ProfileHook &h = profile_hook();
     h.begin = static_cast<cudaEvent_t>(begin_event);
     h.end = static_cast<cudaEvent_t>(end_event);
@@ -263,6 +263,65 @@ int spd_pack_tokens(const int32_t *tokens, const int32_t *doc_lens, int64_t num_
     a.vec_out = aligned(input_ids, 16) && aligned(labels, 16) && aligned(indexes, 16);
     a.vec_in = aligned(tokens, 16);
     return cuda_rc(launch_pack(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int spd_unpack_data(const int32_t *input_ids, const int32_t *labels, const int32_t *cu_seqlens,
+                    const int32_t *row_seg_ptr, int64_t rows, int micro_bsz, int seq_len, int32_t *out_ids,
+                    int32_t *out_labels, spd_stream_t stream)
+{
+    if (micro_bsz < 1 || seq_len < 1 || rows < 0) return SPD_ERR_INVALID_ARG;
+    const int64_t total = rows * static_cast<int64_t>(micro_bsz) * seq_len;
+    if (total > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (rows == 0) return SPD_OK;
+    const void *ptrs[] = {input_ids, labels, cu_seqlens, row_seg_ptr, out_ids, out_labels};
+    for (const void *p : ptrs)
+        if (!p || !aligned(p, 4)) return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    UnpackArgs a = {};
+    a.input_ids = input_ids;
+    a.labels = labels;
+    a.cu_seqlens = cu_seqlens;
+    a.row_seg_ptr = row_seg_ptr;
+    a.rows = static_cast<int32_t>(rows);
+    a.micro_bsz = micro_bsz;
+    a.seq_len = seq_len;
+    a.out_ids = out_ids;
+    a.out_labels = out_labels;
+    a.vec_out = aligned(out_ids, 16) && aligned(out_labels, 16);
+    return cuda_rc(launch_unpack(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const int32_t *src2, int64_t rows,
+                                int64_t len, int sp_size, int rank, int32_t *dst0, int32_t *dst1, int32_t *dst2,
+                                spd_stream_t stream)
+{
+    if (sp_size < 1 || rank < 0 || rank >= sp_size || rows < 0 || len < 0) return SPD_ERR_INVALID_ARG;
+    if (len % sp_size != 0 || rows * len > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    const int32_t *src[3] = {src0, src1, src2};
+    int32_t *dst[3] = {dst0, dst1, dst2};
+    SplitArgs a = {};
+    bool vec = (len / sp_size) % 4 == 0;
+    for (int i = 0; i < 3; ++i) {
+        if ((src[i] == nullptr) != (dst[i] == nullptr)) return SPD_ERR_INVALID_ARG;
+        if (!src[i]) continue;
+        if (!aligned(src[i], 4) || !aligned(dst[i], 4)) return SPD_ERR_INVALID_ARG;
+        vec = vec && aligned(src[i], 16) && aligned(dst[i], 16);
+        a.src[a.n_tensors] = src[i];
+        a.dst[a.n_tensors] = dst[i];
+        ++a.n_tensors;
+    }
+    if (rows == 0 || len == 0 || a.n_tensors == 0) return SPD_OK;
+    int sms = 0;
+    int rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    a.rows = static_cast<int32_t>(rows);
+    a.len = static_cast<int32_t>(len);
+    a.sp_size = sp_size;
+    a.rank = rank;
+    a.vec = vec ? 1 : 0;
+    return cuda_rc(launch_split(a, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t spd_attn_workspace_size(int64_t total_tokens, int32_t num_segs, int Hq, int Hkv, int head_dim, int bwd)

@@ -1,0 +1,117 @@
+// Data steps after packing (InternEvo page "Data loading and flow", section
+// "Processing data"):
+//   unpack_data                   packed rows -> [rows][micro_bsz][seq_len], one
+//                                 segment (document) per output row, cut to
+//                                 seq_len, padded with 0 / -100;
+//   split_data_sequence_parallel  the rank's contiguous 1/sp_size chunk of the
+//                                 sequence dimension of each row.
+// Both are pure data movement (HBM-bound): every thread takes groups of four
+// consecutive output positions, grid-stride, with 16-byte stores where the
+// output row layout allows.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace spd {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int32_t kPad = 0, kIgnore = -100;
+
+__global__ void __launch_bounds__(kThreads) unpack_kernel(UnpackArgs a)
+{
+    const int32_t plen = a.micro_bsz * a.seq_len;
+    const int32_t total = a.rows * plen;
+    const bool vec = a.vec_out && (a.seq_len & 3) == 0;   // a group of 4 never crosses an output row
+    for (int32_t x = (blockIdx.x * kThreads + threadIdx.x) * 4; x < total; x += gridDim.x * kThreads * 4) {
+        int32_t id[4], lab[4];
+        int32_t cur_key = -1, a0 = 0, n = 0;   // segment of the last output row looked up
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            id[k] = kPad;
+            lab[k] = kIgnore;
+            const int32_t p = x + k;
+            if (p >= total) continue;
+            const int32_t r = p / plen, rem = p - r * plen;
+            const int32_t m = rem / a.seq_len, j = rem - m * a.seq_len;
+            const int32_t key = r * a.micro_bsz + m;
+            if (key != cur_key) {          // output row (r, m) <- segment row_seg_ptr[r] + m of row r
+                cur_key = key;
+                const int32_t s = a.row_seg_ptr[r] + m;
+                if (s < a.row_seg_ptr[r + 1]) {
+                    a0 = a.cu_seqlens[s];
+                    n = min(a.cu_seqlens[s + 1] - a0, a.seq_len);
+                } else {
+                    a0 = 0;
+                    n = 0;
+                }
+            }
+            if (j < n) {
+                id[k] = a.input_ids[a0 + j];
+                lab[k] = a.labels[a0 + j];
+            }
+        }
+        if (vec) {
+            *reinterpret_cast<int4 *>(a.out_ids + x) = make_int4(id[0], id[1], id[2], id[3]);
+            *reinterpret_cast<int4 *>(a.out_labels + x) = make_int4(lab[0], lab[1], lab[2], lab[3]);
+        } else {
+            for (int k = 0; k < 4 && x + k < total; ++k) {
+                a.out_ids[x + k] = id[k];
+                a.out_labels[x + k] = lab[k];
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a)
+{
+    const int32_t chunk = a.len / a.sp_size;
+    const int32_t total = a.rows * chunk;
+    const int32_t off = a.rank * chunk;
+    for (int32_t x = (blockIdx.x * kThreads + threadIdx.x) * 4; x < total; x += gridDim.x * kThreads * 4) {
+        const int32_t r = x / chunk, j = x - r * chunk;
+        const int32_t src = r * a.len + off + j;
+        for (int t = 0; t < a.n_tensors; ++t) {
+            if (a.vec && x + 4 <= total) {   // chunk % 4 == 0: the group stays in one row
+                *reinterpret_cast<int4 *>(a.dst[t] + x) = *reinterpret_cast<const int4 *>(a.src[t] + src);
+            } else {
+                for (int k = 0; k < 4 && x + k < total; ++k) {
+                    const int32_t rr = (x + k) / chunk, jj = (x + k) - rr * chunk;
+                    a.dst[t][x + k] = a.src[t][rr * a.len + off + jj];
+                }
+            }
+        }
+    }
+}
+
+unsigned grid_for(int64_t groups, int num_sms)
+{
+    long long blocks = (groups + kThreads - 1) / kThreads;
+    const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return static_cast<unsigned>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_unpack(const UnpackArgs &a, int num_sms, cudaStream_t stream)
+{
+    const int64_t total = static_cast<int64_t>(a.rows) * a.micro_bsz * a.seq_len;
+    if (total == 0) return cudaSuccess;
+    prof_begin(kProfUnpack, stream);
+    unpack_kernel<<<grid_for((total + 3) / 4, num_sms), kThreads, 0, stream>>>(a);
+    prof_end(kProfUnpack, stream);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split(const SplitArgs &a, int num_sms, cudaStream_t stream)
+{
+    const int64_t total = static_cast<int64_t>(a.rows) * (a.len / a.sp_size);
+    if (total == 0 || a.n_tensors == 0) return cudaSuccess;
+    prof_begin(kProfSplit, stream);
+    split_kernel<<<grid_for((total + 3) / 4, num_sms), kThreads, 0, stream>>>(a);
+    prof_end(kProfSplit, stream);
+    return cudaGetLastError();
+}
+
+}  // namespace spd

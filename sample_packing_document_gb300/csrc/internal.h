@@ -12,7 +12,7 @@ namespace spd {
 // Measurement hook (spd_set_profile_events): when `which` names a kernel,
 // its launcher records `begin` / `end` on the launch stream around that one
 // kernel. Per host thread.
-enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3 };
+enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3, kProfUnpack = 4, kProfSplit = 5 };
 struct ProfileHook {
     cudaEvent_t begin = nullptr, end = nullptr;
     int which = kProfNone;
@@ -71,6 +71,25 @@ struct PackArgs {
 
 size_t pack_ws_bytes(int64_t num_docs);
 cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- data steps after packing
+struct UnpackArgs {
+    const int32_t *input_ids, *labels;     // packed rows [rows * micro_bsz * seq_len]
+    const int32_t *cu_seqlens, *row_seg_ptr;
+    int32_t rows, micro_bsz, seq_len;
+    int32_t *out_ids, *out_labels;         // [rows][micro_bsz][seq_len]
+    int vec_out;                           // 1: outputs 16-byte aligned
+};
+cudaError_t launch_unpack(const UnpackArgs &a, int num_sms, cudaStream_t stream);
+
+struct SplitArgs {
+    const int32_t *src[3];
+    int32_t *dst[3];
+    int n_tensors;
+    int32_t rows, len, sp_size, rank;
+    int vec;                               // 1: 16-byte copies (aligned pointers, chunk % 4 == 0)
+};
+cudaError_t launch_split(const SplitArgs &a, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tile schedule
 // One work tile: a 128-token block of one segment. Sorted by cost, largest

@@ -36,6 +36,8 @@ SIGNATURES = {
                                    _P, _P, _P, _P, _SZ, _P]),
     "spd_varlen_attn_fwd_noalloc": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _P, _P, _P,
                                            _P]),
+    "spd_unpack_data": (_INT, [_P, _P, _P, _P, _I64, _INT, _INT, _P, _P, _P]),
+    "spd_split_sequence_parallel": (_INT, [_P, _P, _P, _I64, _I64, _INT, _INT, _P, _P, _P, _P]),
 }
 
 
@@ -99,7 +101,7 @@ def read_status(ws, stream=None):
     return v.value
 
 
-PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD = 0, 1, 2, 3
+PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD, PROFILE_UNPACK, PROFILE_SPLIT = 0, 1, 2, 3, 4, 5
 
 
 def set_profile_events(begin, end, kernel):
@@ -160,6 +162,42 @@ def pack_tokens(tokens, doc_lens, micro_bsz, seq_len, use_packed_dataset=True, o
         _ptr(tokens), _ptr(doc_lens), nd, nt, int(micro_bsz), int(seq_len), int(bool(use_packed_dataset)),
         _ptr(out["input_ids"]), _ptr(out["labels"]), _ptr(out["indexes"]), _ptr(out["cu_seqlens"]),
         _ptr(out["row_seg_ptr"]), _ptr(out["max_seqlen"]), _ptr(out["num_segs"]), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def unpack_data(input_ids, labels, cu_seqlens, row_seg_ptr, rows, micro_bsz, seq_len, out_ids=None,
+                out_labels=None, stream=None):
+    """spd_unpack_data: packed rows (as pack_tokens wrote them, use_packed_dataset
+    False) -> (ids, labels) int32 [rows, micro_bsz, seq_len]."""
+    _need_cuda(input_ids, labels, cu_seqlens, row_seg_ptr)
+    shape = (int(rows), int(micro_bsz), int(seq_len))
+    if out_ids is None:
+        out_ids = torch.empty(shape, dtype=torch.int32, device=input_ids.device)
+    if out_labels is None:
+        out_labels = torch.empty(shape, dtype=torch.int32, device=input_ids.device)
+    _check("spd_unpack_data", load().spd_unpack_data(
+        _ptr(input_ids), _ptr(labels), _ptr(cu_seqlens), _ptr(row_seg_ptr), int(rows), int(micro_bsz),
+        int(seq_len), _ptr(out_ids), _ptr(out_labels), _stream(stream)))
+    return out_ids, out_labels
+
+
+def split_sequence_parallel(tensors, sp_size, rank, out=None, stream=None):
+    """spd_split_sequence_parallel: up to three int32 CUDA tensors [rows, len]
+    (or [len]) -> this rank's [rows, len / sp_size] chunks."""
+    tensors = list(tensors)
+    if not 1 <= len(tensors) <= 3:
+        raise ValueError("one to three tensors")
+    _need_cuda(*tensors)
+    shp = tensors[0].shape
+    rows, n = (1, shp[0]) if len(shp) == 1 else (shp[0], shp[1])
+    if out is None:
+        oshape = (n // sp_size,) if len(shp) == 1 else (rows, n // sp_size)
+        out = [torch.empty(oshape, dtype=torch.int32, device=tensors[0].device) for _ in tensors]
+    src = [_ptr(x) for x in tensors] + [None] * (3 - len(tensors))
+    dst = [_ptr(x) for x in out] + [None] * (3 - len(out))
+    _check("spd_split_sequence_parallel", load().spd_split_sequence_parallel(
+        src[0], src[1], src[2], int(rows), int(n), int(sp_size), int(rank), dst[0], dst[1], dst[2],
         _stream(stream)))
     return out
 

@@ -92,3 +92,19 @@ def test_debug_skip_hook_validates_its_argument():
     assert lib.spd_debug_skip_arrive(-1) == -1
     assert lib.spd_debug_skip_arrive(ops.DEBUG_SKIP_FWD_Q) == 0
     assert lib.spd_debug_skip_arrive(ops.DEBUG_SKIP_NONE) == 0   # cleared again
+
+
+def test_data_steps_host_checks_without_gpu(lib):
+    """Argument checks of the data-step entry points run before any GPU call."""
+    import ctypes
+    P = ctypes.c_void_p
+    one = P(16)
+    # unpack: micro_bsz / seq_len must be >= 1; rows == 0 is a no-op
+    assert lib.spd_unpack_data(one, one, one, one, 1, 0, 8, one, one, None) == -1
+    assert lib.spd_unpack_data(one, one, one, one, 1, 2, 0, one, one, None) == -1
+    assert lib.spd_unpack_data(one, one, one, one, 0, 2, 8, one, one, None) == 0
+    # split: len must divide by sp_size, rank in range, src / dst paired
+    assert lib.spd_split_sequence_parallel(one, None, None, 2, 10, 4, 0, one, None, None, None) == -1
+    assert lib.spd_split_sequence_parallel(one, None, None, 2, 8, 4, 4, one, None, None, None) == -1
+    assert lib.spd_split_sequence_parallel(one, one, None, 2, 8, 4, 0, one, None, None, None) == -1
+    assert lib.spd_split_sequence_parallel(one, None, None, 0, 8, 4, 0, one, None, None, None) == 0

@@ -62,6 +62,15 @@ def test_split_sequence_parallel_worked_example():
         assert P.split_sequence_parallel(b["labels"][0], s["sp_size"], r) == want["labels"]
 
 
+def test_split_after_unpack_worked_example():
+    """The page's second split example: tp size 2 over the unpacked batch."""
+    g, s = GOLDEN["unpack_data"], GOLDEN["split_sequence_parallel_unpacked"]
+    for r in range(s["sp_size"]):
+        want = s["rank%d" % r]
+        assert [P.split_sequence_parallel(row, s["sp_size"], r) for row in g["unpacked_input_ids"]] == want["input_ids"]
+        assert [P.split_sequence_parallel(row, s["sp_size"], r) for row in g["unpacked_labels"]] == want["labels"]
+
+
 def test_flat_layout_worked_example():
     g = GOLDEN["build_pack"]
     f = P.pack_flat(g["docs"], g["micro_bsz"], g["seq_len"], True)
