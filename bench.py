@@ -409,6 +409,7 @@ def main():
     fwd_tf = fl["fwd"] / (fwd_ms * 1e-3) / 1e12
 
     pack = pack_measure(ops, dev) if rank == 0 else None
+    data_steps = data_measure(ops, dev) if rank == 0 else None
 
     e2e = None
     if not args.no_e2e:
@@ -428,7 +429,7 @@ def main():
                 "flops_per_step": fl["total"], "strict_flops_value": ws_n * fl["strict_total"] / (ms * 1e-3) / 1e12,
                 "kernels_ms": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms},
                 "kernels_tflops": {"attn_fwd": fwd_tf, "attn_bwd": bwd_tf},
-                "roofline": roofline, "pack_tokens": pack, "clocks": clocks, "e2e": e2e,
+                "roofline": roofline, "pack_tokens": pack, "data_steps": data_steps, "clocks": clocks, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
                 "cpu_baseline": cpu}
         print(json.dumps(line))
@@ -436,6 +437,62 @@ def main():
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def _time_kernel(ops, which, fn, flush, reps):
+    """Median device time (ms) of the one library kernel `which` that fn()
+    launches, L2 flushed before every repetition."""
+    import torch
+    times = []
+    for it in range(reps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        b.record()
+        ops.set_profile_events(a, b, which)
+        fn()
+        ops.set_profile_events(None, None, ops.PROFILE_NONE)
+        torch.cuda.synchronize()
+        if it >= 3:
+            times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def data_measure(ops, dev, reps=20):
+    """The data steps after packing, each alone on device-resident inputs:
+    spd_unpack_data on the c3 documents packed with use_packed_dataset=False
+    (micro_bsz 4, SEQ_LEN 8192) and spd_split_sequence_parallel of the c5 packed
+    row (input_ids, indexes, labels) at sp_size 8. Algorithmic bytes / time."""
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    pk, how = peaks()
+    hbm = pk.get("hbm_gbs", 6800.0)
+    out = {}
+    # the unpack inputs are the library's own pack of the c3 documents (use_packed_dataset=False)
+    w, lens, toks = workload_docs("c3_unpack")
+    packed = ops.pack_tokens(torch.tensor(toks, dtype=torch.int32, device=dev),
+                             torch.tensor(lens, dtype=torch.int32, device=dev), w.micro_bsz, w.seq_len, False)
+    ids, labs, cu, rsp = packed["input_ids"], packed["labels"], packed["cu_seqlens"], packed["row_seg_ptr"]
+    rows = packed["rows"]
+    o_ids = torch.empty((rows, w.micro_bsz, w.seq_len), dtype=torch.int32, device=dev)
+    o_lab = torch.empty_like(o_ids)
+    ms = _time_kernel(ops, ops.PROFILE_UNPACK, lambda: ops.unpack_data(ids, labs, cu, rsp, rows, w.micro_bsz,
+                                                                       w.seq_len, o_ids, o_lab), flush, reps)
+    kept = int(sum(min(int(n), w.seq_len) for n in lens))
+    nbytes = int(8 * kept + 8 * o_ids.numel() + 4 * (2 * rows * w.micro_bsz + rows + 1))
+    out["unpack_data"] = {"workload": "c3 documents, use_packed_dataset=False: %d rows x %d x %d" % (
+        rows, w.micro_bsz, w.seq_len), "ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+        "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    T, sp = 1 << 20, 8
+    src = [torch.randint(0, 50000, (1, T), dtype=torch.int32, device=dev) for _ in range(3)]
+    dst = [torch.empty((1, T // sp), dtype=torch.int32, device=dev) for _ in range(3)]
+    ms = _time_kernel(ops, ops.PROFILE_SPLIT, lambda: ops.split_sequence_parallel(src, sp, 3, out=dst), flush, reps)
+    nbytes = 3 * 2 * 4 * (T // sp)
+    out["split_sequence_parallel"] = {"workload": "c5 packed row (input_ids, indexes, labels), %d tokens, sp_size %d,"
+                                      " rank 3" % (T, sp), "ms": ms, "bytes": nbytes,
+                                      "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    out["timing"] = "CUDA events recorded by the library around the kernel, L2 flushed, median of %d" % reps
+    return out
 
 
 def pack_measure(ops, dev, name="c5", reps=20):
