@@ -20,4 +20,5 @@ Contents
                tiny inputs; the independent cross-check of ``attn_ref.c``.
 ``tiles``      the tile classification of the block-diagonal causal mask
                (skip / partial / full) and the visited-tile count.
+``rope``       rotary position embedding with per-document positions (fp64).
 """
