@@ -491,6 +491,20 @@ def data_measure(ops, dev, reps=20):
     out["split_sequence_parallel"] = {"workload": "c5 packed row (input_ids, indexes, labels), %d tokens, sp_size %d,"
                                       " rank 3" % (T, sp), "ms": ms, "bytes": nbytes,
                                       "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    # RoPE in place on the c2 batch's q and k (32 + 32 heads x 32768 tokens x 128), positions restarting
+    # at every document (the library's pack of the c2 documents gives them as indexes)
+    w, lens, toks = workload_docs("c2")
+    packed = ops.pack_tokens(torch.tensor(toks, dtype=torch.int32, device=dev),
+                             torch.tensor(lens, dtype=torch.int32, device=dev), w.micro_bsz, w.seq_len, True)
+    pos = packed["indexes"]
+    T = pos.numel()
+    q = torch.randn((T, w.Hq, w.head_dim), device=dev).to(torch.bfloat16)
+    k = torch.randn((T, w.Hkv, w.head_dim), device=dev).to(torch.bfloat16)
+    ms = _time_kernel(ops, ops.PROFILE_ROPE, lambda: ops.rope(q, k, pos), flush, reps)
+    nbytes = 2 * 2 * (w.Hq + w.Hkv) * T * w.head_dim + 4 * T
+    out["rope"] = {"workload": "c2 q / k in place: %d tokens, %d + %d heads, d %d, positions = indexes" % (
+        T, w.Hq, w.Hkv, w.head_dim), "ms": ms, "bytes": int(nbytes), "GB/s": nbytes / (ms * 1e-3) / 1e9,
+        "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
     out["timing"] = "CUDA events recorded by the library around the kernel, L2 flushed, median of %d" % reps
     return out
 

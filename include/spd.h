@@ -87,7 +87,8 @@ enum {
     SPD_PROFILE_ATTN_FWD = 2,
     SPD_PROFILE_ATTN_BWD = 3,
     SPD_PROFILE_UNPACK = 4,   /* the kernel of spd_unpack_data */
-    SPD_PROFILE_SPLIT = 5     /* the kernel of spd_split_sequence_parallel */
+    SPD_PROFILE_SPLIT = 5,    /* the kernel of spd_split_sequence_parallel */
+    SPD_PROFILE_ROPE = 6      /* the kernel of spd_rope */
 };
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel);
 
@@ -218,6 +219,25 @@ int spd_unpack_data(const int32_t *input_ids, const int32_t *labels, const int32
 int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const int32_t *src2, int64_t rows,
                                 int64_t len, int sp_size, int rank, int32_t *dst0, int32_t *dst1, int32_t *dst2,
                                 spd_stream_t stream);
+
+/*
+ * Rotary position embedding with per-document positions, in place (the
+ * attention-layer pseudo code under Figure 1 of the XTuner page "序列并行"
+ * applies it to q and k before attention; positions are the pack's `indexes`,
+ * restarting at every document: page "Sample Packing ...", section 4.1,
+ * reset_position_id). Rotate-half form: channel j < d/2 of every head is
+ * paired with channel j + d/2 and turned by p * theta_j, theta_j =
+ * rope_theta^(-2j/d) (rope_theta <= 0: 10000); inverse != 0 turns by
+ * -p * theta_j, which maps dq / dk of the rotated tensors back to the inputs.
+ *
+ * q bf16 [T, Hq, head_dim], k bf16 [T, Hkv, head_dim], rotated in place; either
+ * may be NULL. positions int32 [T], each >= 0 (indexes of spd_pack_tokens).
+ * head_dim 64 or 128. The angle is exact to ~1e-9 rad for any int32 position.
+ * Returns SPD_ERR_INVALID_ARG (bad sizes, q / k not 16-byte aligned, positions
+ * NULL while T > 0), SPD_ERR_UNSUPPORTED or SPD_ERR_CUDA.
+ */
+int spd_rope(uint16_t *q, uint16_t *k, const int32_t *positions, int64_t total_tokens, int Hq, int Hkv,
+             int head_dim, float rope_theta, int inverse, spd_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Attention                                                                 */

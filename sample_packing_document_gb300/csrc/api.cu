@@ -181,7 +181,7 @@ int spd_debug_skip_arrive(int which)
 
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel)
 {
-    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_SPLIT) return SPD_ERR_INVALID_ARG;
+    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_ROPE) return SPD_ERR_INVALID_ARG;
     ProfileHook &h = profile_hook();
     h.begin = static_cast<cudaEvent_t>(begin_event);
     h.end = static_cast<cudaEvent_t>(end_event);
@@ -322,6 +322,37 @@ int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const 
     a.rank = rank;
     a.vec = vec ? 1 : 0;
     return cuda_rc(launch_split(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int spd_rope(uint16_t *q, uint16_t *k, const int32_t *positions, int64_t total_tokens, int Hq, int Hkv,
+             int head_dim, float rope_theta, int inverse, spd_stream_t stream)
+{
+    if (head_dim != 64 && head_dim != 128) return SPD_ERR_UNSUPPORTED;
+    if (total_tokens < 0 || total_tokens > 0x7fffffffLL || Hq < 0 || Hkv < 0) return SPD_ERR_INVALID_ARG;
+    if ((q && Hq == 0) || (k && Hkv == 0)) return SPD_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(Hq > Hkv ? Hq : Hkv) * total_tokens * head_dim > (1LL << 40)) return SPD_ERR_INVALID_ARG;
+    if ((q && !aligned(q, 16)) || (k && !aligned(k, 16))) return SPD_ERR_INVALID_ARG;
+    if (total_tokens == 0 || (!q && !k)) return SPD_OK;
+    if (!positions || !aligned(positions, 4)) return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    RopeArgs a = {};
+    a.q = q;
+    a.k = k;
+    a.pos = positions;
+    a.T = static_cast<int32_t>(total_tokens);
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = head_dim;
+    a.inverse = inverse ? 1 : 0;
+    const double base = rope_theta > 0.f ? static_cast<double>(rope_theta) : 10000.0;
+    for (int j = 0; j < head_dim / 2; ++j) {
+        // turns per position, theta_j / (2 pi) < 1/6, as 64-bit fixed point
+        const double turns = std::pow(base, -2.0 * j / head_dim) / (2.0 * 3.141592653589793238462643);
+        a.freq[j] = static_cast<unsigned long long>(std::ldexp(turns, 64));
+    }
+    return cuda_rc(launch_rope(a, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t spd_attn_workspace_size(int64_t total_tokens, int32_t num_segs, int Hq, int Hkv, int head_dim, int bwd)

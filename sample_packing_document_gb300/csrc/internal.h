@@ -12,7 +12,7 @@ namespace spd {
 // Measurement hook (spd_set_profile_events): when `which` names a kernel,
 // its launcher records `begin` / `end` on the launch stream around that one
 // kernel. Per host thread.
-enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3, kProfUnpack = 4, kProfSplit = 5 };
+enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3, kProfUnpack = 4, kProfSplit = 5, kProfRope = 6 };
 struct ProfileHook {
     cudaEvent_t begin = nullptr, end = nullptr;
     int which = kProfNone;
@@ -90,6 +90,16 @@ struct SplitArgs {
     int vec;                               // 1: 16-byte copies (aligned pointers, chunk % 4 == 0)
 };
 cudaError_t launch_split(const SplitArgs &a, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- rotary position embedding
+struct RopeArgs {
+    uint16_t *q, *k;                 // bf16 [T, Hq, d] / [T, Hkv, d], in place (either may be null)
+    const int32_t *pos;              // [T] positions (>= 0)
+    int32_t T, Hq, Hkv, d;
+    int inverse;                     // 1: rotate by -angle
+    unsigned long long freq[64];     // turns per position of pair j as 64-bit fixed point (j < d/2)
+};
+cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tile schedule
 // One work tile: a 128-token block of one segment. Sorted by cost, largest

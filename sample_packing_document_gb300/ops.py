@@ -38,6 +38,7 @@ SIGNATURES = {
                                            _P]),
     "spd_unpack_data": (_INT, [_P, _P, _P, _P, _I64, _INT, _INT, _P, _P, _P]),
     "spd_split_sequence_parallel": (_INT, [_P, _P, _P, _I64, _I64, _INT, _INT, _P, _P, _P, _P]),
+    "spd_rope": (_INT, [_P, _P, _P, _I64, _INT, _INT, _INT, _F32, _INT, _P]),
 }
 
 
@@ -101,7 +102,8 @@ def read_status(ws, stream=None):
     return v.value
 
 
-PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD, PROFILE_UNPACK, PROFILE_SPLIT = 0, 1, 2, 3, 4, 5
+(PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD, PROFILE_UNPACK, PROFILE_SPLIT,
+ PROFILE_ROPE) = 0, 1, 2, 3, 4, 5, 6
 
 
 def set_profile_events(begin, end, kernel):
@@ -200,6 +202,21 @@ def split_sequence_parallel(tensors, sp_size, rank, out=None, stream=None):
         src[0], src[1], src[2], int(rows), int(n), int(sp_size), int(rank), dst[0], dst[1], dst[2],
         _stream(stream)))
     return out
+
+
+def rope(q, k, positions, rope_theta=None, inverse=False, stream=None):
+    """spd_rope: rotate q [T, Hq, d] and / or k [T, Hkv, d] (bf16 CUDA tensors,
+    either may be None) in place by the per-token positions (int32 [T], e.g.
+    the pack's indexes). inverse=True applies the transposed rotation (the
+    gradient map). Returns (q, k)."""
+    _need_cuda(q, k, positions)
+    ref = q if q is not None else k
+    T, _, d = ref.shape
+    Hq = q.shape[1] if q is not None else 0
+    Hkv = k.shape[1] if k is not None else 0
+    _check("spd_rope", load().spd_rope(_ptr(q), _ptr(k), _ptr(positions), int(T), int(Hq), int(Hkv), int(d),
+                                       float(rope_theta or 0.0), int(bool(inverse)), _stream(stream)))
+    return q, k
 
 
 # ----------------------------------------------------------------------------- attention

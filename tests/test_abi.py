@@ -108,3 +108,13 @@ def test_data_steps_host_checks_without_gpu(lib):
     assert lib.spd_split_sequence_parallel(one, None, None, 2, 8, 4, 4, one, None, None, None) == -1
     assert lib.spd_split_sequence_parallel(one, one, None, 2, 8, 4, 0, one, None, None, None) == -1
     assert lib.spd_split_sequence_parallel(one, None, None, 0, 8, 4, 0, one, None, None, None) == 0
+
+
+def test_rope_host_checks_without_gpu(lib):
+    """spd_rope's argument checks run before any GPU call."""
+    import ctypes
+    P = ctypes.c_void_p
+    assert lib.spd_rope(P(16), None, P(16), 4, 2, 0, 96, ctypes.c_float(0), 0, None) == -2   # head_dim
+    assert lib.spd_rope(P(18), None, P(16), 4, 2, 0, 128, ctypes.c_float(0), 0, None) == -1  # alignment
+    assert lib.spd_rope(P(16), None, None, 4, 2, 0, 128, ctypes.c_float(0), 0, None) == -1   # positions
+    assert lib.spd_rope(P(16), None, P(16), 0, 2, 0, 128, ctypes.c_float(0), 0, None) == 0   # T = 0
