@@ -21,4 +21,6 @@ Contents
 ``tiles``      the tile classification of the block-diagonal causal mask
                (skip / partial / full) and the visited-tile count.
 ``rope``       rotary position embedding with per-document positions (fp64).
+``loss``       masked token cross-entropy over packed labels, its gradient and the
+               sequence-parallel token-weighted reduction (fp64).
 """
