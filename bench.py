@@ -505,6 +505,21 @@ def data_measure(ops, dev, reps=20):
     out["rope"] = {"workload": "c2 q / k in place: %d tokens, %d + %d heads, d %d, positions = indexes" % (
         T, w.Hq, w.Hkv, w.head_dim), "ms": ms, "bytes": int(nbytes), "GB/s": nbytes / (ms * 1e-3) / 1e9,
         "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    # masked token loss and its gradient over the c2 batch's labels (the same pack), synthetic bf16 logits
+    # over a 50000-token vocabulary (the token ids' range)
+    V = 50000
+    labels = packed["labels"]
+    logits = (torch.randn((T, V), device=dev) * 2).to(torch.bfloat16)
+    dlogits = torch.empty_like(logits)
+    tok_loss = torch.empty(T, dtype=torch.float32, device=dev)
+    ms = _time_kernel(ops, ops.PROFILE_LOSS, lambda: ops.masked_token_loss(logits, labels, dlogits=dlogits,
+                                                                           grad_scale=1.0 / T, token_loss=tok_loss),
+                      flush, reps)
+    nbytes = 2 * 2 * T * V + 12 * T
+    out["masked_token_loss"] = {"workload": "c2 labels (%d tokens) with bf16 logits over %d classes, loss + gradient"
+                                % (T, V), "ms": ms, "bytes": int(nbytes), "GB/s": nbytes / (ms * 1e-3) / 1e9,
+                                "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    del logits, dlogits
     out["timing"] = "CUDA events recorded by the library around the kernel, L2 flushed, median of %d" % reps
     return out
 

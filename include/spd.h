@@ -88,7 +88,8 @@ enum {
     SPD_PROFILE_ATTN_BWD = 3,
     SPD_PROFILE_UNPACK = 4,   /* the kernel of spd_unpack_data */
     SPD_PROFILE_SPLIT = 5,    /* the kernel of spd_split_sequence_parallel */
-    SPD_PROFILE_ROPE = 6      /* the kernel of spd_rope */
+    SPD_PROFILE_ROPE = 6,     /* the kernel of spd_rope */
+    SPD_PROFILE_LOSS = 7      /* the row kernel of spd_masked_token_loss */
 };
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel);
 
@@ -238,6 +239,30 @@ int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const 
  */
 int spd_rope(uint16_t *q, uint16_t *k, const int32_t *positions, int64_t total_tokens, int Hq, int Hkv,
              int head_dim, float rope_theta, int inverse, spd_stream_t stream);
+
+/*
+ * Masked token loss over packed labels (XTuner page "序列并行", section
+ * "Reduce Loss": the rank's loss is the mean token cross-entropy over labels
+ * that are not -100; num_tokens = (labels != -100).sum() weighs it in
+ * reduce_sequence_parallel_loss). For token t with a counted label:
+ * token_loss[t] = logsumexp(logits[t]) - logits[t][label] (natural log, fp32);
+ * ignored tokens (label -100) get 0. *loss_sum (fp64) is the sum over tokens in
+ * a fixed order (reproducible), *num_tokens the count of counted tokens; the
+ * caller forms the mean loss_sum / num_tokens, or the token-weighted mean over
+ * sequence-parallel ranks. If dlogits is not NULL it receives
+ * (softmax(logits[t]) - onehot(label)) * grad_scale (bf16), zero rows for
+ * ignored tokens (grad_scale = 1 / total counted tokens for the mean).
+ *
+ * logits bf16 [T, V], labels int32 [T] (the pack's labels), token_loss fp32
+ * [T], loss_sum double [1], num_tokens int32 [1], dlogits bf16 [T, V] or NULL,
+ * device_status int32 [1] or NULL: receives SPD_ERR_INVALID_ARG if a label is
+ * outside [0, V) and not -100 (that token then counts for nothing; the caller
+ * clears the word before the call). Returns SPD_ERR_INVALID_ARG (bad sizes,
+ * null or unaligned pointers), SPD_ERR_UNSUPPORTED or SPD_ERR_CUDA.
+ */
+int spd_masked_token_loss(const uint16_t *logits, const int32_t *labels, int64_t T, int64_t V, float *token_loss,
+                          double *loss_sum, int32_t *num_tokens, uint16_t *dlogits, float grad_scale,
+                          int32_t *device_status, spd_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Attention                                                                 */

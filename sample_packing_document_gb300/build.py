@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
-SOURCES = ["api.cu", "pack.cu", "data.cu", "rope.cu", "sched.cu", "attn_fwd.cu", "attn_bwd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "pack.cu", "data.cu", "rope.cu", "loss.cu", "sched.cu", "attn_fwd.cu", "attn_bwd.cu",
+           "noalloc.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 

@@ -181,7 +181,7 @@ int spd_debug_skip_arrive(int which)
 
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel)
 {
-    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_ROPE) return SPD_ERR_INVALID_ARG;
+    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_LOSS) return SPD_ERR_INVALID_ARG;
     ProfileHook &h = profile_hook();
     h.begin = static_cast<cudaEvent_t>(begin_event);
     h.end = static_cast<cudaEvent_t>(end_event);
@@ -353,6 +353,35 @@ int spd_rope(uint16_t *q, uint16_t *k, const int32_t *positions, int64_t total_t
         a.freq[j] = static_cast<unsigned long long>(std::ldexp(turns, 64));
     }
     return cuda_rc(launch_rope(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int spd_masked_token_loss(const uint16_t *logits, const int32_t *labels, int64_t T, int64_t V, float *token_loss,
+                          double *loss_sum, int32_t *num_tokens, uint16_t *dlogits, float grad_scale,
+                          int32_t *device_status, spd_stream_t stream)
+{
+    if (T < 0 || T > 0x7fffffffLL || V < 1 || V > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (!loss_sum || !num_tokens || !aligned(loss_sum, 8) || !aligned(num_tokens, 4)) return SPD_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !labels || !token_loss)) return SPD_ERR_INVALID_ARG;
+    const void *p4[] = {labels, token_loss, device_status};
+    for (const void *p : p4)
+        if (p && !aligned(p, 4)) return SPD_ERR_INVALID_ARG;
+    if ((logits && !aligned(logits, 2)) || (dlogits && !aligned(dlogits, 2))) return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    LossArgs a = {};
+    a.logits = logits;
+    a.labels = labels;
+    a.T = static_cast<int32_t>(T);
+    a.V = static_cast<int32_t>(V);
+    a.token_loss = token_loss;
+    a.loss_sum = loss_sum;
+    a.num_tokens = num_tokens;
+    a.dlogits = dlogits;
+    a.grad_scale = grad_scale;
+    a.status = device_status;
+    a.vec = V % 8 == 0 && aligned(logits, 16) && (!dlogits || aligned(dlogits, 16));
+    return cuda_rc(launch_loss(a, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t spd_attn_workspace_size(int64_t total_tokens, int32_t num_segs, int Hq, int Hkv, int head_dim, int bwd)

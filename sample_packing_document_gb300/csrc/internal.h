@@ -12,7 +12,7 @@ namespace spd {
 // Measurement hook (spd_set_profile_events): when `which` names a kernel,
 // its launcher records `begin` / `end` on the launch stream around that one
 // kernel. Per host thread.
-enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3, kProfUnpack = 4, kProfSplit = 5, kProfRope = 6 };
+enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3, kProfUnpack = 4, kProfSplit = 5, kProfRope = 6, kProfLoss = 7 };
 struct ProfileHook {
     cudaEvent_t begin = nullptr, end = nullptr;
     int which = kProfNone;
@@ -100,6 +100,21 @@ struct RopeArgs {
     unsigned long long freq[64];     // turns per position of pair j as 64-bit fixed point (j < d/2)
 };
 cudaError_t launch_rope(const RopeArgs &a, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- masked token loss
+struct LossArgs {
+    const uint16_t *logits;          // bf16 [T, V]
+    const int32_t *labels;           // [T], -100 = not counted
+    int32_t T, V;
+    float *token_loss;               // [T]
+    double *loss_sum;                // [1]
+    int32_t *num_tokens;             // [1]
+    uint16_t *dlogits;               // bf16 [T, V] or null
+    float grad_scale;
+    int32_t *status;                 // [1] or null: SPD_ERR_INVALID_ARG on a label outside [0, V)
+    int vec;                         // 1: rows in 16-byte chunks (V % 8 == 0, aligned pointers)
+};
+cudaError_t launch_loss(const LossArgs &a, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tile schedule
 // One work tile: a 128-token block of one segment. Sorted by cost, largest

@@ -8,6 +8,7 @@
 namespace spd {
 
 // Status word codes written by kernels (mirrors include/spd.h).
+constexpr int kErrInvalidArg = -1;
 constexpr int kErrBadSeqlens = -4;
 constexpr int kErrTimeout = -5;
 constexpr int kErrBadDocs = -7;

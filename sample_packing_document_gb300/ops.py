@@ -39,6 +39,7 @@ SIGNATURES = {
     "spd_unpack_data": (_INT, [_P, _P, _P, _P, _I64, _INT, _INT, _P, _P, _P]),
     "spd_split_sequence_parallel": (_INT, [_P, _P, _P, _I64, _I64, _INT, _INT, _P, _P, _P, _P]),
     "spd_rope": (_INT, [_P, _P, _P, _I64, _INT, _INT, _INT, _F32, _INT, _P]),
+    "spd_masked_token_loss": (_INT, [_P, _P, _I64, _I64, _P, _P, _P, _P, _F32, _P, _P]),
 }
 
 
@@ -103,7 +104,7 @@ def read_status(ws, stream=None):
 
 
 (PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD, PROFILE_UNPACK, PROFILE_SPLIT,
- PROFILE_ROPE) = 0, 1, 2, 3, 4, 5, 6
+ PROFILE_ROPE, PROFILE_LOSS) = 0, 1, 2, 3, 4, 5, 6, 7
 
 
 def set_profile_events(begin, end, kernel):
@@ -217,6 +218,23 @@ def rope(q, k, positions, rope_theta=None, inverse=False, stream=None):
     _check("spd_rope", load().spd_rope(_ptr(q), _ptr(k), _ptr(positions), int(T), int(Hq), int(Hkv), int(d),
                                        float(rope_theta or 0.0), int(bool(inverse)), _stream(stream)))
     return q, k
+
+
+def masked_token_loss(logits, labels, dlogits=None, grad_scale=0.0, token_loss=None, device_status=None,
+                      stream=None):
+    """spd_masked_token_loss: logits bf16 [T, V], labels int32 [T] CUDA tensors.
+    Returns (token_loss fp32 [T], loss_sum fp64 [1], num_tokens int32 [1]) on the
+    device; dlogits (bf16 [T, V]) is filled when given."""
+    _need_cuda(logits, labels, dlogits, device_status)
+    T, V = logits.shape
+    if token_loss is None:
+        token_loss = torch.empty(T, dtype=torch.float32, device=logits.device)
+    loss_sum = torch.empty(1, dtype=torch.float64, device=logits.device)
+    num_tokens = torch.empty(1, dtype=torch.int32, device=logits.device)
+    _check("spd_masked_token_loss", load().spd_masked_token_loss(
+        _ptr(logits), _ptr(labels), int(T), int(V), _ptr(token_loss), _ptr(loss_sum), _ptr(num_tokens),
+        _ptr(dlogits), float(grad_scale), _ptr(device_status), _stream(stream)))
+    return token_loss, loss_sum, num_tokens
 
 
 # ----------------------------------------------------------------------------- attention

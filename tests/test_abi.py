@@ -118,3 +118,15 @@ def test_rope_host_checks_without_gpu(lib):
     assert lib.spd_rope(P(18), None, P(16), 4, 2, 0, 128, ctypes.c_float(0), 0, None) == -1  # alignment
     assert lib.spd_rope(P(16), None, None, 4, 2, 0, 128, ctypes.c_float(0), 0, None) == -1   # positions
     assert lib.spd_rope(P(16), None, P(16), 0, 2, 0, 128, ctypes.c_float(0), 0, None) == 0   # T = 0
+
+
+def test_loss_host_checks_without_gpu(lib):
+    """spd_masked_token_loss's argument checks run before any GPU call."""
+    import ctypes
+    P = ctypes.c_void_p
+    assert lib.spd_masked_token_loss(P(16), P(16), 4, 0, P(16), P(16), P(16), None, ctypes.c_float(0), None,
+                                     None) == -1   # V < 1
+    assert lib.spd_masked_token_loss(P(16), P(16), 4, 8, P(16), None, P(16), None, ctypes.c_float(0), None,
+                                     None) == -1   # no loss_sum
+    assert lib.spd_masked_token_loss(P(16), P(16), 4, 8, P(16), P(12), P(16), None, ctypes.c_float(0), None,
+                                     None) == -1   # loss_sum not 8-byte aligned
