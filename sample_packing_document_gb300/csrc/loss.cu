@@ -9,6 +9,8 @@
 // log2 e), the CTA combines them, loss = (lse2 - y[label]) * ln 2. With a
 // gradient buffer, a second pass over the row (still in L2) writes
 // (softmax - onehot(label)) * grad_scale as bf16.
+// loss_row_smem_kernel: the same with the row staged in shared memory by one
+// bulk copy (vocabularies up to 57344): HBM sees each logit once.
 // loss_sum_kernel: one CTA sums the per-token losses in fp64 in a fixed order
 // (deterministic) and counts the tokens.
 #include "internal.h"
@@ -129,6 +131,104 @@ __global__ void __launch_bounds__(kRowThreads) loss_row_kernel(LossArgs a)
     }
 }
 
+// The same with the row staged once in shared memory by a bulk copy (rows of
+// at most kSmemRowMax bf16, 16-byte aligned): both passes read shared memory,
+// so HBM sees every logit once even when the gradient is written.
+constexpr int kSmemRowMax = 56 * 1024;   // 112 KB of bf16: two CTAs per SM
+
+__global__ void __launch_bounds__(kRowThreads) loss_row_smem_kernel(LossArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem_row[];
+    __shared__ float sm_m[kRowThreads / 32], sm_s[kRowThreads / 32];
+    __shared__ float row_lse2;
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint16_t *srow = reinterpret_cast<const uint16_t *>(smem_row);
+    const uint32_t row_bytes = static_cast<uint32_t>(a.V) * 2;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t loads = 0;
+    int dummy_status = 0;
+    for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+        const int32_t lab = a.labels[t];
+        uint16_t *grow = a.dlogits ? a.dlogits + static_cast<size_t>(t) * a.V : nullptr;
+        if (lab == kIgnore || lab < 0 || lab >= a.V) {
+            if (tid == 0) {
+                a.token_loss[t] = 0.f;
+                if (lab != kIgnore && a.status) atomicExch(a.status, kErrInvalidArg);
+            }
+            zero_row(grow, a.V, tid);
+            continue;
+        }
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bar, row_bytes);
+            bulk_load(smem_row, a.logits + static_cast<size_t>(t) * a.V, row_bytes, &bar);
+        }
+        // bounded wait; a copy that never lands leaves the row's loss at 0
+        const bool ok = mbar_wait(&bar, loads & 1, &abort_flag, a.status ? a.status : &dummy_status);
+        ++loads;
+        if (!__syncthreads_and(ok)) break;
+        float m = -INFINITY, s = 0.f;
+        for (int i = tid * 8; i < a.V; i += kRowThreads * 8) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(srow + i);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            float y[8], cm = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                y[2 * e] = __uint_as_float(ww[e] << 16) * kLog2e;
+                y[2 * e + 1] = __uint_as_float(ww[e] & 0xffff0000u) * kLog2e;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cm = fmaxf(cm, y[e]);
+            float cs = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cs += ex2(y[e] - cm);
+            lse_combine(m, s, cm, cs);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            lse_combine(m, s, m2, s2);
+        }
+        if (lane == 0) {
+            sm_m[warp] = m;
+            sm_s[warp] = s;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float M = sm_m[0], S = sm_s[0];
+            for (int w = 1; w < kRowThreads / 32; ++w) lse_combine(M, S, sm_m[w], sm_s[w]);
+            const float lse2 = M + __log2f(S);
+            row_lse2 = lse2;
+            a.token_loss[t] = (lse2 - bf16_to_f(srow[lab]) * kLog2e) * kLn2;
+        }
+        __syncthreads();
+        if (grow) {
+            const float lse2 = row_lse2, sc = a.grad_scale;
+            for (int i = tid * 8; i < a.V; i += kRowThreads * 8) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(srow + i);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = i + 2 * e;
+                    const float p0 = ex2(__uint_as_float(ww[e] << 16) * kLog2e - lse2) - (j == lab ? 1.f : 0.f);
+                    const float p1 = ex2(__uint_as_float(ww[e] & 0xffff0000u) * kLog2e - lse2) -
+                                     (j + 1 == lab ? 1.f : 0.f);
+                    o[e] = pack_bf16x2(p0 * sc, p1 * sc);
+                }
+                *reinterpret_cast<uint4 *>(grow + i) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        __syncthreads();   // the next row's copy overwrites the staged row
+    }
+}
+
 __global__ void __launch_bounds__(kSumThreads) loss_sum_kernel(LossArgs a)
 {
     __shared__ double sh_s[kSumThreads / 32];
@@ -171,9 +271,18 @@ cudaError_t launch_loss(const LossArgs &a, int num_sms, cudaStream_t stream)
         long long blocks = a.T;
         const long long cap = static_cast<long long>(num_sms > 0 ? num_sms : 1) * 8;
         if (blocks > cap) blocks = cap;
-        prof_begin(kProfLoss, stream);
-        loss_row_kernel<<<static_cast<unsigned>(blocks), kRowThreads, 0, stream>>>(a);
-        prof_end(kProfLoss, stream);
+        if (a.vec && a.V <= kSmemRowMax) {
+            const int smem = a.V * 2;
+            cudaError_t e = cudaFuncSetAttribute(loss_row_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            prof_begin(kProfLoss, stream);
+            loss_row_smem_kernel<<<static_cast<unsigned>(blocks), kRowThreads, smem, stream>>>(a);
+            prof_end(kProfLoss, stream);
+        } else {
+            prof_begin(kProfLoss, stream);
+            loss_row_kernel<<<static_cast<unsigned>(blocks), kRowThreads, 0, stream>>>(a);
+            prof_end(kProfLoss, stream);
+        }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

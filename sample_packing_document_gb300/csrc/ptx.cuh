@@ -130,6 +130,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, int
         : "memory");
 }
 
+// Contiguous bulk copy global -> shared (both 16-byte aligned, bytes a multiple
+// of 16), completing on an mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // 3-D tiled reduce-add (fp32 add) of a shared-memory tile into global memory,
 // tracked by this thread's bulk-async group.
 __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *m, const void *src, int c0, int c1, int c2)
