@@ -17,8 +17,9 @@
 //                    TMEM region, rescales O_X in TMEM when needed, final
 //                    normalisation and stores.
 //   warp 8           TMA producer: takes the next work unit, loads Q_A, Q_B and
-//                    streams the K / V tiles through a 2-stage ring that runs
-//                    on across units.
+//                    streams the K / V tiles through 2-stage rings that run on
+//                    across units, K one tile ahead of V (a K stage frees after
+//                    the last S MMA reading it, a step before its V stage).
 //   warp 9           MMA issuer: S_X(j) = Q_X K_j^T (both operands in shared
 //                    memory), O_X += P_X(j) V_j (P from TMEM, V from shared
 //                    memory), interleaved A / B so one tile's softmax overlaps
@@ -51,7 +52,7 @@ struct alignas(1024) FwdSmem {
     uint8_t v[kStages][D / 64][kAtom];
     uint8_t ostage[8][32 * 128];   // per softmax warp: 32 rows x 64 d of O (bf16, 128-byte swizzle)
     uint64_t q_full, q_empty;
-    uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+    uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t unit_full[2], unit_empty[2];
     int4 unit[2];               // work unit in flight: {head (-1: no more work), seg_start, seg_end, first tile}
@@ -108,7 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.k_full[s], 1);
             mbar_init(&sm.v_full[s], 1);
-            mbar_init(&sm.kv_empty[s], 1);
+            mbar_init(&sm.k_empty[s], 1);
+            mbar_init(&sm.v_empty[s], 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
@@ -151,9 +153,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // then head-major (the CTAs on one head run together, so the K / V tiles
         // they share stay in L2), longest first inside a head.
         if (lane == 0) {
-            uint32_t kv_iter = 0;
-            int last_kv_use[kStages] = {-1, -1};
+            // K runs one kv tile ahead of V: a K stage frees as soon as the last S
+            // MMA reading it has completed (one kv step before its V stage), so the
+            // copy of K(n + 2) starts a step earlier than a shared K / V stage would
+            // allow. V(n) is issued right after K(n + 1).
+            uint32_t kv_iter = 0;              // global index of the next K tile
+            int last_k_use[kStages] = {-1, -1}, last_v_use[kStages] = {-1, -1};
+            int pend_v = -1, pend_row = 0, pend_g = 0;   // a V tile not yet issued
             int q_loads = 0;
+            auto load_v = [&](int n, int row, int g) -> bool {
+                const int st = n % kStages, use = n / kStages;
+                if (use > 0 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, a.status)) return false;
+                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.v[st][c], &a.tm_v, c * 64, g, row, &sm.v_full[st]);
+                last_v_use[st] = use;
+                return true;
+            };
             for (int it = 0;; ++it) {
                 const int slot = it & 1;
                 if (it >= 2 && !mbar_wait(&sm.unit_empty[slot], ((it >> 1) - 1) & 1, abort_flag, a.status)) break;
@@ -167,7 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 }
                 sm.unit[slot] = d;
                 mbar_arrive(&sm.unit_full[slot]);
-                if (d.x < 0) break;
+                if (d.x < 0) {
+                    if (pend_v >= 0 && !*abort_flag) load_v(pend_v, pend_row, pend_g);   // the last V tile
+                    break;
+                }
                 const UnitShape us = unit_shape(d);
                 const int h = d.x, g = h / (a.Hq / a.Hkv);
                 const int q0A = d.y + us.tA * kTile;
@@ -183,26 +201,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 bool ok = true;
                 for (int j = 0; j < us.n_kv; ++j, ++kv_iter) {
                     const int st = kv_iter % kStages, use = kv_iter / kStages;
-                    if (use > 0 && !mbar_wait(&sm.kv_empty[st], (use - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                    if (use > 0 && !mbar_wait(&sm.k_empty[st], (use - 1) & 1, abort_flag, a.status)) { ok = false; break; }
                     const int kv0 = d.y + j * kTile;
                     mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
                     for (int c = 0; c < D / 64; ++c)
                         tma_load_3d(sm.k[st][c], &a.tm_k, c * 64, g, kv0, &sm.k_full[st]);
-                    mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-                    for (int c = 0; c < D / 64; ++c)
-                        tma_load_3d(sm.v[st][c], &a.tm_v, c * 64, g, kv0, &sm.v_full[st]);
-                    last_kv_use[st] = use;
+                    last_k_use[st] = use;
+                    if (pend_v >= 0 && !load_v(pend_v, pend_row, pend_g)) { ok = false; break; }
+                    pend_v = static_cast<int>(kv_iter);
+                    pend_row = kv0;
+                    pend_g = g;
                 }
                 if (!ok) break;
             }
             if (*abort_flag) {
                 // Let the copies still in flight land before the CTA exits.
                 if (q_loads > 0) wait_drain(&sm.q_full, (q_loads - 1) & 1);
-                for (int s = 0; s < kStages; ++s)
-                    if (last_kv_use[s] >= 0) {
-                        wait_drain(&sm.k_full[s], last_kv_use[s] & 1);
-                        wait_drain(&sm.v_full[s], last_kv_use[s] & 1);
-                    }
+                for (int s = 0; s < kStages; ++s) {
+                    if (last_k_use[s] >= 0) wait_drain(&sm.k_full[s], last_k_use[s] & 1);
+                    if (last_v_use[s] >= 0) wait_drain(&sm.v_full[s], last_v_use[s] & 1);
+                }
             }
         }
     } else if (warp == 9) {
@@ -211,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             constexpr uint32_t idesc_s = idesc_bf16(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16(128, D, 0, 1);
             uint32_t kv_iter = 0;
-            int empty_commits[kStages] = {0, 0};
+            int k_commits[kStages] = {0, 0}, v_commits[kStages] = {0, 0};
             int q_commits = 0;
             uint32_t p_cnt0 = 0, p_cnt1 = 0;      // P tiles consumed, per q tile slot
             uint32_t o_cnt0 = 0, o_cnt1 = 0;      // units that used O_A / O_B
@@ -253,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 tc_fence_after();
                 issue_s(0, 0);                        // S regions: the last P V of each tile ran before
                 if (n_tile1 > 0) issue_s(1, 0);
+                umma_commit(&sm.k_empty[kv_iter % kStages]);   // K(0) read by both tiles' first S
+                ++k_commits[kv_iter % kStages];
                 for (int j = 0; ok && j < us.n_kv; ++j) {
                     const uint32_t kvj = kv_iter + j;
                     const int st = kvj % kStages;
@@ -287,8 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&sm.kv_empty[st]);
-                    ++empty_commits[st];
+                    if (next_k) {                     // K(j + 1) read by every S of this step
+                        umma_commit(&sm.k_empty[(kvj + 1) % kStages]);
+                        ++k_commits[(kvj + 1) % kStages];
+                    }
+                    umma_commit(&sm.v_empty[st]);     // V(j) read by every P V of this step
+                    ++v_commits[st];
                 }
                 kv_iter += us.n_kv;
             }
@@ -296,8 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             // before the CTA exits.
             umma_commit(&sm.drain);
             wait_drain(&sm.drain, 0);
-            for (int s = 0; s < kStages; ++s)
-                if (empty_commits[s] > 0) wait_drain(&sm.kv_empty[s], (empty_commits[s] - 1) & 1);
+            for (int s = 0; s < kStages; ++s) {
+                if (k_commits[s] > 0) wait_drain(&sm.k_empty[s], (k_commits[s] - 1) & 1);
+                if (v_commits[s] > 0) wait_drain(&sm.v_empty[s], (v_commits[s] - 1) & 1);
+            }
             if (q_commits > 0) wait_drain(&sm.q_empty, (q_commits - 1) & 1);
         }
     }
