@@ -114,9 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
-            mbar_init(&sm.p_full[x], 128);
+            mbar_init(&sm.p_full[x], 4);      // one arrive per softmax warp
             mbar_init(&sm.o_done[x], 1);
-            mbar_init(&sm.o_free[x], 128);
+            mbar_init(&sm.o_free[x], 4);
             mbar_init(&sm.unit_full[x], 1);
             mbar_init(&sm.unit_empty[x], 9);   // MMA thread + one lane of each softmax warp
         }
@@ -416,7 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 l += (sums[0] + sums[1]) + (sums[2] + sums[3]);
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&sm.p_full[x]);
+                __syncwarp();                 // the warp's P stores are done: one arrive for all 32 lanes
+                if (lane == 0) mbar_arrive(&sm.p_full[x]);
             }
             if (!ok) break;
             // epilogue: normalise O_X and store it with the row's LSE. O is read
@@ -442,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             pack_bf16x2(__uint_as_float(o[h2][2 * e]) * inv_l, __uint_as_float(o[h2][2 * e + 1]) * inv_l);
             }
             tc_fence_before();
-            mbar_arrive(&sm.o_free[x]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.o_free[x]);
             if (valid) a.lse[static_cast<size_t>(h) * a.total_tokens + qi] = (m + log2f(l)) * 0.69314718055994531f;
             // A quarter wholly inside the segment leaves through TMA stores of
             // [32 rows][64 d] boxes staged in this warp's slot (whole lines in HBM);
