@@ -515,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int col0 = half * 64;                               // this warp's 64 q columns
         const float sl2 = a.scale_log2;
+        const uint64_t sl2_2 = f2_pack(sl2, sl2);
         const uint32_t ds_addr = smem_u32(sm.ds[0]);
         const bool loader = half == 0;                            // loads the step's LSE / D column t
         auto col_term = [&](const int4 &u, int i) -> float {
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             const int qi = u.y + (u.w + i % nq) * kTile + t;
             if (qi >= a.total_tokens) return 0.f;
             const size_t x = static_cast<size_t>(h) * a.total_tokens + qi;
-            return is_p ? a.lse[x] * 1.4426950408889634f : a.delta[x];
+            return is_p ? -a.lse[x] * 1.4426950408889634f : a.delta[x];   // P warps keep -LSE log2 e
         };
         // dS warps' staging slots: A in the step's spent Q stage (d = 128), B in
         // the dS buffer (free once dK / dQ, its readers, have completed).
@@ -591,13 +592,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                         uint32_t pk[16];
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
-                            const float4 l4 = CC[c * 8 + e4];   // one broadcast load for four columns
-                            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                            const float4 l4 = CC[c * 8 + e4];   // one broadcast load for four columns (-LSE log2 e)
+                            const uint64_t lv2[2] = {f2_pack(l4.x, l4.y), f2_pack(l4.z, l4.w)};
 #pragma unroll
                             for (int e2 = 0; e2 < 2; ++e2) {
                                 const int e = e4 * 2 + e2, col = c * 32 + 2 * e;
-                                float p0 = ex2(__uint_as_float(sv[2 * e]) * sl2 - lv[2 * e2]);
-                                float p1 = ex2(__uint_as_float(sv[2 * e + 1]) * sl2 - lv[2 * e2 + 1]);
+                                // the scale and the LSE of a column pair in one packed instruction
+                                float p0, p1;
+                                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
+                                                 sl2_2, lv2[e2]),
+                                          p0, p1);
+                                p0 = ex2(p0);
+                                p1 = ex2(p1);
                                 if (!full) {
                                     if (col < c_lo || col >= c_hi) p0 = 0.f;
                                     if (col + 1 < c_lo || col + 1 >= c_hi) p1 = 0.f;
@@ -635,12 +641,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
 #pragma unroll
                         for (int e4 = 0; e4 < 8; ++e4) {
                             const float4 d4 = CC[c * 8 + e4];
-                            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+                            const uint64_t dv2[2] = {f2_pack(d4.x, d4.y), f2_pack(d4.z, d4.w)};
 #pragma unroll
                             for (int e2 = 0; e2 < 2; ++e2) {
                                 const int e = e4 * 2 + e2;
-                                const float d0 = bf16_lo(pv[e]) * (__uint_as_float(dp[2 * e]) - dv4[2 * e2]);
-                                const float d1 = bf16_hi(pv[e]) * (__uint_as_float(dp[2 * e + 1]) - dv4[2 * e2 + 1]);
+                                // dS = P (dP - D) for a column pair, two packed instructions
+                                float d0, d1;
+                                f2_unpack(f2_mul(f2_pack(bf16_lo(pv[e]), bf16_hi(pv[e])),
+                                                 f2_sub(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                                        dv2[e2])),
+                                          d0, d1);
                                 pk[e] = pack_bf16x2(d0, d1);
                             }
                         }

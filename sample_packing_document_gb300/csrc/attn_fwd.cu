@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 uint32_t sv[128];
                 tmem_ld128(tmem + lane_off + s_col, sv);
                 tmem_wait_ld();
-                // row max, 8 independent chains
+                // row max: 8 independent chains of three-input maxima
                 float mxs[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) mxs[e] = -INFINITY;
@@ -369,10 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         if (e <= r) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 128; ++e) mxs[e & 7] = fmaxf(mxs[e & 7], __uint_as_float(sv[e]));
+                    for (int e = 0; e < 128; e += 16)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            mxs[c] = fmax3(mxs[c], __uint_as_float(sv[e + c]), __uint_as_float(sv[e + 8 + c]));
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mxs[0], mxs[1]), fmaxf(mxs[2], mxs[3])),
-                                       fmaxf(fmaxf(mxs[4], mxs[5]), fmaxf(mxs[6], mxs[7])));
+                const float mx = fmaxf(fmax3(mxs[0], mxs[1], mxs[2]), fmax3(mxs[3], mxs[4], fmax3(mxs[5], mxs[6], mxs[7])));
                 const float m_new = fmaxf(m, mx * sl2);
                 const bool need = m_new > m + 8.0f;
                 if (__any_sync(0xffffffffu, need)) {
@@ -394,26 +396,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     m = m_use;
                 }
                 // P = 2^(S * scale * log2 e - m), written as bf16 over the first 64
-                // columns of S_X's region (already in registers).
-                float sums[4] = {0.f, 0.f, 0.f, 0.f};
+                // columns of S_X's region (already in registers). Columns go in
+                // pairs through the packed fp32 instructions (half the issue slots
+                // of scalar ones: the loop is bound by instruction issue).
+                const uint64_t sl2_2 = f2_pack(sl2, sl2), negm_2 = f2_pack(-m, -m);
+                uint64_t sum2[2] = {0ull, 0ull};   // (0.f, 0.f)
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int col = c * 32 + 2 * e;
-                        float p0 = ex2(__uint_as_float(sv[col]) * sl2 - m);
-                        float p1 = ex2(__uint_as_float(sv[col + 1]) * sl2 - m);
+                        const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])),
+                                                   sl2_2, negm_2);
+                        float p0, p1;
+                        f2_unpack(x2, p0, p1);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
                         if (diag) {
                             if (col > r) p0 = 0.f;
                             if (col + 1 > r) p1 = 0.f;
                         }
-                        sums[e & 3] += p0 + p1;
+                        sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
                         pk[e] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16(tmem + lane_off + s_col + c * 16, pk);
                 }
-                l += (sums[0] + sums[1]) + (sums[2] + sums[3]);
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(sum2[0], a0, a1);
+                    f2_unpack(sum2[1], b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();                 // the warp's P stores are done: one arrive for all 32 lanes
