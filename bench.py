@@ -48,6 +48,46 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# Sources the main backward kernel is compiled from: a recorded DRAM-traffic
+# figure is reported only while their hash matches the one the capture recorded.
+BWD_SOURCES = ("attn_bwd.cu", "ptx.cuh", "internal.h")
+
+
+def kernel_source_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "sample_packing_document_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(summary, files, w):
+    """DRAM bytes per launch of a kernel from its ncu summary under profiles/:
+    the summary states the source hash it was captured at, the bytes per launch
+    and the head count of the captured workload (same documents, fewer heads;
+    traffic grows with the heads, which are independent). None when the file
+    is missing or the kernel's sources changed since."""
+    try:
+        with open(os.path.join(ROOT, "profiles", summary)) as f:
+            text = f.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if line.startswith("traffic-record:"):
+            for kv in line.split(":", 1)[1].split():
+                k, _, v = kv.partition("=")
+                fields[k] = v
+    try:
+        if (fields["source"] != kernel_source_hash(files) or fields["docs"] != w.docs_name
+                or int(fields["group"]) != w.Hq // w.Hkv or int(fields["d"]) != w.head_dim):
+            return None
+        return int(fields["dram_bytes"]) * w.Hq // int(fields["hq"])
+    except (KeyError, ValueError):
+        return None
+
+
 def workload_docs(name):
     from sample_packing_document_gb300 import workloads as W
     w = W.WORKLOADS[name]
@@ -403,7 +443,9 @@ def main():
     bwd_tf = fl["bwd"] / (bwd_ms * 1e-3) / 1e12
     roofline = {"kernel": "attn_bwd_kernel (main backward kernel, %d%% of step time)" % round(100 * bwd_ms / ms),
                 "bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
-                "frac": bwd_tf / peak, "traffic": None,
+                "frac": bwd_tf / peak, "traffic": recorded_traffic("attn_bwd_c2p.md", BWD_SOURCES, w),
+                "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch, profiles/attn_bwd_c2p.md, "
+                                  "scaled by the head count (null once the kernel's sources change)",
                 "peak_source": "%s bf16_tflops_sustained (kernel timed inside the step loop)" % how,
                 "flops_per_launch": fl["bwd"], "ms_per_launch": bwd_ms}
     fwd_tf = fl["fwd"] / (fwd_ms * 1e-3) / 1e12

@@ -48,6 +48,11 @@ class Workload:
     Hkv: int
     head_dim: int
     q_scale: float = 1.0
+    docs: str = ""        # name of the workload whose documents these are (default: this one)
+
+    @property
+    def docs_name(self):
+        return self.docs or self.name
 
 
 WORKLOADS = {
@@ -60,7 +65,7 @@ WORKLOADS = {
     "c5": Workload("c5", 4, 1, 1048576, True, 1048576, 4, 4, 128),
     # c2's documents with 16 / 16 heads: a smaller device footprint for
     # hardware-counter captures (inputs still larger than L2).
-    "c2p": Workload("c2p", 1, 2, 4096, True, 32768, 16, 16, 128),
+    "c2p": Workload("c2p", 1, 2, 4096, True, 32768, 16, 16, 128, docs="c2"),
 }
 
 
