@@ -142,6 +142,40 @@ def test_mid_size_full_compare(ops):
     _check_full(ops, lens, 4, 2, 128, seed=8)
 
 
+def test_backward_workspace_reuse(ops):
+    """One backward workspace used again and again: repeated calls, a call of
+    another shape (the workspace regions move), the first shape again, and a
+    workspace full of garbage must all match the oracle (nothing a call leaves
+    behind in the workspace may leak into the next)."""
+    Hq, Hkv, d = 4, 2, 128
+    shapes = ([300, 1, 129, 517], [700, 260])
+    size = max(ops.attn_workspace_size(sum(l), len(l), Hq, Hkv, d, True) for l in shapes)
+    ws_b = ops.workspace(size)
+    cases = []
+    for n, lens in enumerate(shapes):
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T = int(cu[-1])
+        q, k, v, do = _inputs(T, Hq, Hkv, d, 30 + n)
+        cu_t = torch.tensor(cu, device="cuda")
+        ws_f = ops.workspace(ops.attn_workspace_size(T, len(lens), Hq, Hkv, d, False))
+        out, lse = ops.varlen_attn_fwd(q, k, v, cu_t, len(lens), ws=ws_f)
+        ref = OA.attn_bwd(_u16(q), _u16(k), _u16(v), _u16(do), cu)[:3]
+        cases.append((q, k, v, do, out, lse, cu_t, len(lens), ref))
+
+    def check(c):
+        q, k, v, do, out, lse, cu_t, ns, ref = c
+        g = ops.varlen_attn_bwd(q, k, v, out, do, lse, cu_t, ns, grad_dtype=torch.float32, ws=ws_b)
+        assert ops.read_status(ws_b) == 0
+        for x, r in zip(g, ref):
+            assert _maxerr(x.float().cpu().numpy(), r) <= TOL_G
+
+    for c in (cases[0], cases[0], cases[0], cases[1], cases[1], cases[0]):
+        check(c)
+    ws_b.fill_(0x7f)           # memory used for something else in between
+    check(cases[1])
+    check(cases[1])
+
+
 def test_bad_seqlens_set_status(ops):
     q, k, v, do = _inputs(512, 2, 2, 128, 1)
     for cu in ([0, 300, 200, 512], [0, 300, 511], [1, 300, 512], [0, 300, 300, 512]):
