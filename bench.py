@@ -276,7 +276,25 @@ def cpu_baseline(w, seg_lens, target_s=12.0):
     f = 14.0 * w.head_dim * w.Hq * pairs
     return {"value": f / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "fp64 oracle fwd+bwd over %d whole segments (%.3g of %.3g unmasked pairs, all %d heads), %.1f s"
-                      % (len(segs), pairs, float(np.sum(seg_lens * (seg_lens + 1.0) / 2)), w.Hq, t)}
+                      % (len(segs), pairs, float(np.sum(seg_lens * (seg_lens + 1.0) / 2)), w.Hq, t),
+            "pack": cpu_pack_baseline()}
+
+
+def cpu_pack_baseline(name="c5", reps=5):
+    """The pack oracle's C twin (sequential, one core) on the workload the GPU
+    pack is measured on, in the same algorithmic bytes."""
+    from oracle import attention as OA
+    w, lens, toks = workload_docs(name)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        r = OA.pack(toks, lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
+        times.append(time.perf_counter() - t0)
+    npos = r["rows"] * w.micro_bsz * w.seq_len
+    nbytes = 4 * len(toks) + 4 * len(lens) + 12 * npos + 4 * (r["num_segs"] + 1) + 4 * (2 * r["rows"] + 2)
+    s = statistics.median(times)
+    return {"GB/s": nbytes / s / 1e9, "ms": s * 1e3, "bytes": nbytes, "cores": 1, "kind": "oracle (C twin of the rules)",
+            "sample": "%s documents: %d tokens, %d documents, median of %d calls" % (name, len(toks), len(lens), reps)}
 
 
 def run_reference(args):
@@ -340,6 +358,9 @@ def main():
     ap.add_argument("--workload", default="c2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["pack", "data"], default=None,
+                    help="run only the pack (c5 documents) or the data-step measurements and print their JSON "
+                         "(for profiling those kernels without the attention step)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -356,6 +377,10 @@ def main():
     __graft_entry__.build()
     from sample_packing_document_gb300 import ops
     from sample_packing_document_gb300 import workloads as W
+    if args.only:
+        if rank == 0:
+            print(json.dumps(pack_measure(ops, dev) if args.only == "pack" else data_measure(ops, dev)))
+        return 0
 
     w, lens, toks = workload_docs(args.workload)
     seg_lens = segment_lengths(lens, w)

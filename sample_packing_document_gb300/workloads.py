@@ -66,6 +66,9 @@ WORKLOADS = {
     # c2's documents with 16 / 16 heads: a smaller device footprint for
     # hardware-counter captures (inputs still larger than L2).
     "c2p": Workload("c2p", 1, 2, 4096, True, 32768, 16, 16, 128, docs="c2"),
+    # c5's documents with one q / kv head: the million-token row within a few GB
+    # of device memory for hardware-counter captures.
+    "c5p": Workload("c5p", 4, 1, 1048576, True, 1048576, 1, 1, 128, docs="c5"),
 }
 
 
@@ -83,7 +86,7 @@ def _draw_length(name, rng):
         u = rng.random()
         ea, eb = a ** (1 - alpha), b ** (1 - alpha)
         return int(np.floor((ea - u * (ea - eb)) ** (1.0 / (1 - alpha))))
-    if name == "c5":
+    if name in ("c5", "c5p"):
         if rng.random() < 0.95:
             return int(rng.integers(16, 513))
         return int(rng.integers(32768, 131073))
