@@ -630,47 +630,82 @@ def pack_measure(ops, dev, name="c5", reps=20):
 
 
 def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
-    """Same metric through the public API with host buffers: every step copies
-    the documents and q / k / v / dO from pinned host memory, packs, runs
-    forward and backward, and reads dQ / dK / dV back to pinned host memory."""
+    """Same metric through the public API with host buffers, pipelined the way
+    a training loop feeds the GPU: every step copies its documents and q / k /
+    v / dO from pinned host memory (copy stream in), packs and runs forward and
+    backward (compute stream), and reads dQ / dK / dV back to pinned host
+    memory (copy stream out); step k + 1's inputs load and step k - 1's results
+    drain while step k computes (two buffer sets). The segment count comes from
+    the host document lengths (spd_pack_num_segs), so no step waits on the
+    device. Timed from before the first copy in to after the last copy out."""
     import torch
-    h = lambda t: t.cpu().pin_memory()
+    NB = 2
+    ns = ops.pack_num_segs(lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
+    pin = lambda t: t.cpu().pin_memory()
     toks_h, lens_h = torch.tensor(toks).pin_memory(), torch.tensor(lens).pin_memory()
-    q_h, k_h, v_h, do_h = h(q), h(k), h(v), h(do)
-    dq_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-    dk_h = torch.empty(k.shape, dtype=k.dtype).pin_memory()
-    dv_h = torch.empty(v.shape, dtype=v.dtype).pin_memory()
-    d_toks, d_lens = torch.empty_like(toks_h, device=dev), torch.empty_like(lens_h, device=dev)
-    d_q, d_k, d_v, d_do = (torch.empty_like(x, device=dev) for x in (q_h, k_h, v_h, do_h))
+    in_h = (toks_h, lens_h, pin(q), pin(k), pin(v), pin(do))
+    in_d = [tuple(torch.empty_like(x, device=dev) for x in in_h) for _ in range(NB)]
+    out_h = [tuple(torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (q, k, v)) for _ in range(NB)]
+    out_d = [tuple(torch.empty_like(x) for x in (q, k, v)) for _ in range(NB)]
+    pk = ops.alloc_pack_outputs(len(lens), len(toks), w.micro_bsz, w.seq_len, w.use_packed_dataset, dev)
+    T, Hq, Hkv, d = q.shape[0], w.Hq, w.Hkv, w.head_dim
+    o = torch.empty_like(q)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=dev)
+    ws_f = ops.workspace(ops.attn_workspace_size(T, ns, Hq, Hkv, d, False), dev)
+    ws_b = ops.workspace(ops.attn_workspace_size(T, ns, Hq, Hkv, d, True), dev)
+    s_comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_ready, comp_done, out_read = [ev() for _ in range(NB)], [ev() for _ in range(NB)], [ev() for _ in range(NB)]
     seg_lens = segment_lengths(lens, w)
     fl = flops(seg_lens, w.Hq, w.head_dim)
 
-    def one():
-        for dst, src in ((d_toks, toks_h), (d_lens, lens_h), (d_q, q_h), (d_k, k_h), (d_v, v_h), (d_do, do_h)):
-            dst.copy_(src, non_blocking=True)
-        pk = ops.pack_tokens(d_toks, d_lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
-        ns = int(pk["num_segs"].item())
-        o, lse = ops.varlen_attn_fwd(d_q, d_k, d_v, pk["cu_seqlens"], ns)
-        gq, gk, gv = ops.varlen_attn_bwd(d_q, d_k, d_v, o, d_do, lse, pk["cu_seqlens"], ns)
-        dq_h.copy_(gq, non_blocking=True)
-        dk_h.copy_(gk, non_blocking=True)
-        dv_h.copy_(gv, non_blocking=True)
+    def step(kk):
+        b = kk % NB
+        with torch.cuda.stream(s_in):
+            if kk >= NB:
+                s_in.wait_event(comp_done[b])     # step kk - NB has finished reading these inputs
+            for dst, src in zip(in_d[b], in_h):
+                dst.copy_(src, non_blocking=True)
+            in_ready[b].record(s_in)
+        s_comp.wait_event(in_ready[b])
+        if kk >= NB:
+            s_comp.wait_event(out_read[b])        # step kk - NB's results have been read back
+        d_toks, d_lens, d_q, d_k, d_v, d_do = in_d[b]
+        ns = ops.pack_num_segs(lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)   # host: this step's documents
+        ops.pack_tokens(d_toks, d_lens, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk, stream=s_comp)
+        ops.varlen_attn_fwd(d_q, d_k, d_v, pk["cu_seqlens"], ns, out=o, lse=lse, ws=ws_f, stream=s_comp)
+        ops.varlen_attn_bwd(d_q, d_k, d_v, o, d_do, lse, pk["cu_seqlens"], ns, dq=out_d[b][0], dk=out_d[b][1],
+                            dv=out_d[b][2], ws=ws_b, stream=s_comp)
+        comp_done[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[b])
+            for dst, src in zip(out_h[b], out_d[b]):
+                dst.copy_(src, non_blocking=True)
+            out_read[b].record(s_out)
 
-    for _ in range(2):
-        one()
+    for kk in range(2 * NB):
+        step(kk)
     torch.cuda.synchronize()
-    n = max(2, min(args.steps, 5))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n):
-        one()
-    b.record()
+    n = max(4, min(args.steps, 10))
+    a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(s_comp)
+    s_in.wait_event(a)                            # no copy of the timed steps starts before `a`
+    for kk in range(n):
+        step(kk)
+    for bb in range(NB):
+        s_comp.wait_event(out_read[bb])           # every read-back has landed
+    bev.record(s_comp)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / n
-    h2d = sum(x.numel() * x.element_size() for x in (toks_h, lens_h, q_h, k_h, v_h, do_h))
-    d2h = 4 + sum(x.numel() * x.element_size() for x in (dq_h, dk_h, dv_h))
+    if ops.read_status(ws_b) != 0 or ops.read_status(pk["ws"]) != 0:
+        raise RuntimeError("e2e status")
+    ms = a.elapsed_time(bev) / n
+    h2d = sum(x.numel() * x.element_size() for x in in_h)
+    d2h = sum(x.numel() * x.element_size() for x in out_h[0])
     return {"value": fl["total"] / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "%d buffer sets; copies in / compute / copies out on three streams; segment count "
+                        "from the host document lengths" % NB}
 
 
 if __name__ == "__main__":

@@ -136,6 +136,18 @@ int spd_read_status(const void *ws, spd_stream_t stream, int *device_status);
 int spd_pack_rows(int64_t num_docs, int64_t num_tokens, int micro_bsz, int seq_len,
                   int use_packed_dataset, int64_t *rows, int64_t *max_segs);
 
+/*
+ * Host only (no GPU work): the exact number of segments spd_pack_tokens will
+ * write to num_segs for these document lengths (doc_lens: HOST int32
+ * [num_docs], each >= 1), so a caller can size and launch the attention calls
+ * without reading num_segs back from the device. Packed mode: one segment per
+ * row a document spans, plus the padding tail of the last row if it is not
+ * full; unpack mode: each row's documents (cut to seq_len) plus the row's
+ * padding tail if any. SPD_ERR_INVALID_ARG for bad arguments.
+ */
+int spd_pack_num_segs(const int32_t *doc_lens, int64_t num_docs, int micro_bsz, int seq_len,
+                      int use_packed_dataset, int64_t *num_segs);
+
 /* Workspace bytes spd_pack_tokens needs for num_docs documents. */
 size_t spd_pack_workspace_size(int64_t num_docs);
 

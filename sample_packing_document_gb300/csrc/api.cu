@@ -216,6 +216,38 @@ int spd_pack_rows(int64_t num_docs, int64_t num_tokens, int micro_bsz, int seq_l
     return SPD_OK;
 }
 
+int spd_pack_num_segs(const int32_t *doc_lens, int64_t num_docs, int micro_bsz, int seq_len, int use_packed_dataset,
+                      int64_t *num_segs)
+{
+    if (!num_segs || (num_docs > 0 && !doc_lens)) return SPD_ERR_INVALID_ARG;
+    if (micro_bsz <= 0 || seq_len <= 0 || num_docs < 0 || num_docs > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    const int64_t plen = static_cast<int64_t>(micro_bsz) * seq_len;
+    int64_t segs = 0;
+    if (use_packed_dataset) {
+        // one segment per row a document spans, then the padding tail of the last row
+        int64_t start = 0;
+        for (int64_t d = 0; d < num_docs; ++d) {
+            if (doc_lens[d] <= 0) return SPD_ERR_INVALID_ARG;
+            segs += (start + doc_lens[d] - 1) / plen - start / plen + 1;
+            start += doc_lens[d];
+        }
+        if (start % plen != 0) ++segs;
+    } else {
+        // each row: its (at most micro_bsz) documents cut to seq_len, then the padding tail
+        for (int64_t first = 0; first < num_docs; first += micro_bsz) {
+            int64_t kept = 0;
+            for (int64_t d = first; d < num_docs && d < first + micro_bsz; ++d) {
+                if (doc_lens[d] <= 0) return SPD_ERR_INVALID_ARG;
+                kept += doc_lens[d] < seq_len ? doc_lens[d] : seq_len;
+                ++segs;
+            }
+            if (kept < plen) ++segs;
+        }
+    }
+    *num_segs = segs;
+    return SPD_OK;
+}
+
 size_t spd_pack_workspace_size(int64_t num_docs)
 {
     if (num_docs < 0) return 0;

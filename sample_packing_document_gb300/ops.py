@@ -31,6 +31,7 @@ SIGNATURES = {
     "spd_pack_workspace_size": (_SZ, [_I64]),
     "spd_pack_tokens": (_INT, [_P, _P, _I64, _I64, _INT, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "spd_attn_workspace_size": (_SZ, [_I64, _I32, _INT, _INT, _INT, _INT]),
+    "spd_pack_num_segs": (_INT, [_P, _I64, _INT, _INT, _INT, ctypes.POINTER(_I64)]),
     "spd_varlen_attn_fwd": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _P, _P, _P, _SZ, _P]),
     "spd_varlen_attn_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _INT,
                                    _P, _P, _P, _P, _SZ, _P]),
@@ -137,6 +138,18 @@ def pack_rows(num_docs, num_tokens, micro_bsz, seq_len, use_packed_dataset=True)
 
 def pack_workspace_size(num_docs):
     return load().spd_pack_workspace_size(int(num_docs))
+
+
+def pack_num_segs(doc_lens, micro_bsz, seq_len, use_packed_dataset=True):
+    """spd_pack_num_segs on host document lengths (any int sequence): the
+    segment count spd_pack_tokens will produce, without touching the GPU."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(doc_lens, dtype=np.int32))
+    n = _I64(0)
+    _check("spd_pack_num_segs", load().spd_pack_num_segs(lens.ctypes.data_as(ctypes.c_void_p), int(lens.shape[0]),
+                                                         int(micro_bsz), int(seq_len), int(bool(use_packed_dataset)),
+                                                         ctypes.byref(n)))
+    return int(n.value)
 
 
 def alloc_pack_outputs(num_docs, num_tokens, micro_bsz, seq_len, use_packed_dataset=True, device="cuda"):

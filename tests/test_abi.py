@@ -38,6 +38,29 @@ def test_status_strings_and_version(lib):
         assert ops.status_string(code) != "unknown status"
 
 
+def test_pack_num_segs_matches_the_oracle(lib):
+    """The host segment count equals the number of segments the oracle's
+    packing rules produce (which the GPU pack is pinned to bit for bit), in
+    both modes, with documents split across rows, exact row fits and
+    truncation."""
+    import numpy as np
+    from oracle import pack as P
+    from sample_packing_document_gb300 import ops
+    rng = np.random.default_rng(5)
+    cases = [([3, 4, 5, 4], 2, 4), ([8, 8], 2, 4), ([1], 1, 1), ([16], 2, 8), ([17, 1, 30, 2], 2, 8)]
+    for _ in range(60):
+        n = int(rng.integers(1, 30))
+        cases.append((rng.integers(1, 40, size=n).tolist(), int(rng.integers(1, 4)), int(rng.integers(1, 24))))
+    for lens, mb, sl in cases:
+        docs = [[1] * L for L in lens]
+        for packed in (True, False):
+            want = P.pack_flat(docs, mb, sl, packed)["num_segs"]
+            assert ops.pack_num_segs(lens, mb, sl, packed) == want, (lens, mb, sl, packed)
+    assert ops.pack_num_segs([], 2, 8, True) == 0
+    with pytest.raises(ops.SpdError):
+        ops.pack_num_segs([3, 0, 2], 2, 8, True)
+
+
 def test_pack_rows_host_logic(lib):
     from sample_packing_document_gb300 import ops
     assert ops.pack_rows(4, 24, 2, 8, True) == (2, 8)        # the page's example: 2 rows
