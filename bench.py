@@ -632,14 +632,15 @@ def pack_measure(ops, dev, name="c5", reps=20):
 def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
     """Same metric through the public API with host buffers, pipelined the way
     a training loop feeds the GPU: every step copies its documents and q / k /
-    v / dO from pinned host memory (copy stream in), packs and runs forward and
-    backward (compute stream), and reads dQ / dK / dV back to pinned host
-    memory (copy stream out); step k + 1's inputs load and step k - 1's results
-    drain while step k computes (two buffer sets). The segment count comes from
+    v / dO from pinned host memory (copy stream in; dO last, the backward waits
+    for it alone), packs and runs forward and backward (compute stream), and
+    reads dQ / dK / dV back to pinned host memory (copy stream out); the next
+    steps' inputs load and the previous steps' results drain while a step
+    computes (three buffer sets). The segment count comes from
     the host document lengths (spd_pack_num_segs), so no step waits on the
     device. Timed from before the first copy in to after the last copy out."""
     import torch
-    NB = 2
+    NB = 3
     ns = ops.pack_num_segs(lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
     pin = lambda t: t.cpu().pin_memory()
     toks_h, lens_h = torch.tensor(toks).pin_memory(), torch.tensor(lens).pin_memory()
@@ -657,6 +658,7 @@ def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
     in_ready, comp_done, out_read = [ev() for _ in range(NB)], [ev() for _ in range(NB)], [ev() for _ in range(NB)]
+    do_ready = [ev() for _ in range(NB)]
     seg_lens = segment_lengths(lens, w)
     fl = flops(seg_lens, w.Hq, w.head_dim)
 
@@ -665,9 +667,11 @@ def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
         with torch.cuda.stream(s_in):
             if kk >= NB:
                 s_in.wait_event(comp_done[b])     # step kk - NB has finished reading these inputs
-            for dst, src in zip(in_d[b], in_h):
+            for dst, src in zip(in_d[b][:5], in_h[:5]):   # documents, q, k, v: what the pack and forward read
                 dst.copy_(src, non_blocking=True)
             in_ready[b].record(s_in)
+            in_d[b][5].copy_(in_h[5], non_blocking=True)    # dO, read by the backward only
+            do_ready[b].record(s_in)
         s_comp.wait_event(in_ready[b])
         if kk >= NB:
             s_comp.wait_event(out_read[b])        # step kk - NB's results have been read back
@@ -675,6 +679,7 @@ def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
         ns = ops.pack_num_segs(lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)   # host: this step's documents
         ops.pack_tokens(d_toks, d_lens, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk, stream=s_comp)
         ops.varlen_attn_fwd(d_q, d_k, d_v, pk["cu_seqlens"], ns, out=o, lse=lse, ws=ws_f, stream=s_comp)
+        s_comp.wait_event(do_ready[b])
         ops.varlen_attn_bwd(d_q, d_k, d_v, o, d_do, lse, pk["cu_seqlens"], ns, dq=out_d[b][0], dk=out_d[b][1],
                             dv=out_d[b][2], ws=ws_b, stream=s_comp)
         comp_done[b].record(s_comp)
@@ -704,8 +709,8 @@ def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
     d2h = sum(x.numel() * x.element_size() for x in out_h[0])
     return {"value": fl["total"] / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": "%d buffer sets; copies in / compute / copies out on three streams; segment count "
-                        "from the host document lengths" % NB}
+            "pipeline": "%d buffer sets; copies in / compute / copies out on three streams (dO after the "
+                        "forward's inputs); segment count from the host document lengths" % NB}
 
 
 if __name__ == "__main__":
