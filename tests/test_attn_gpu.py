@@ -119,6 +119,12 @@ def test_length_one_documents(ops):
     assert float(dq.abs().max()) < 1e-4 and float(dk.abs().max()) < 1e-4
 
 
+def test_many_segments(ops):
+    """Thousands of segments (4500 one-token documents, then two longer ones):
+    the scheduler's per-segment offsets and search at that count."""
+    _check_full(ops, [1] * 4500 + [300, 129], 2, 2, 64, seed=9)
+
+
 def test_packed_row_from_pack_kernel(ops):
     """The pipeline: pack_tokens' cu_seqlens (documents split across rows and a
     padding tail) feed the attention calls directly."""
