@@ -539,8 +539,10 @@ def _time_kernel(ops, which, fn, flush, reps):
 def data_measure(ops, dev, reps=20):
     """The data steps after packing, each alone on device-resident inputs:
     spd_unpack_data on the c3 documents packed with use_packed_dataset=False
-    (micro_bsz 4, SEQ_LEN 8192) and spd_split_sequence_parallel of the c5 packed
-    row (input_ids, indexes, labels) at sp_size 8. Algorithmic bytes / time."""
+    (micro_bsz 4, SEQ_LEN 8192), spd_split_sequence_parallel of the c5 packed
+    row (input_ids, indexes, labels) at sp_size 8, spd_pad_for_sequence_parallel
+    of a ragged labels row, RoPE and the masked token loss. Algorithmic bytes /
+    time."""
     import torch
     torch.manual_seed(7)       # the random tensors below are seeded like every other input
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -570,6 +572,15 @@ def data_measure(ops, dev, reps=20):
     out["split_sequence_parallel"] = {"workload": "c5 packed row (input_ids, indexes, labels), %d tokens, sp_size %d,"
                                       " rank 3" % (T, sp), "ms": ms, "bytes": nbytes,
                                       "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    # sequence-parallel padding of a ragged row: the c5 row cut to 1048573 tokens, labels padded to sp_size 8
+    T = (1 << 20) - 3
+    lab = torch.randint(-100, 50000, (1, T), dtype=torch.int32, device=dev)
+    ms = _time_kernel(ops, ops.PROFILE_PAD, lambda: ops.pad_for_sequence_parallel(sp, labels=lab), flush, reps)
+    padded = -(-T // sp) * sp
+    nbytes = 4 * T + 4 * padded
+    out["pad_for_sequence_parallel"] = {"workload": "labels row of %d tokens padded to %d (sp_size %d)" % (
+        T, padded, sp), "ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+        "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
     # RoPE in place on the c2 batch's q and k (32 + 32 heads x 32768 tokens x 128), positions restarting
     # at every document (the library's pack of the c2 documents gives them as indexes)
     w, lens, toks = workload_docs("c2")

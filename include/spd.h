@@ -19,7 +19,8 @@
  *
  * and the data steps that follow packing (page "Data loading and flow",
  * section "Processing data"): spd_unpack_data and
- * spd_split_sequence_parallel.
+ * spd_split_sequence_parallel, and the sequence-parallel padding before the
+ * split (spd_pad_for_sequence_parallel).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -89,7 +90,8 @@ enum {
     SPD_PROFILE_UNPACK = 4,   /* the kernel of spd_unpack_data */
     SPD_PROFILE_SPLIT = 5,    /* the kernel of spd_split_sequence_parallel */
     SPD_PROFILE_ROPE = 6,     /* the kernel of spd_rope */
-    SPD_PROFILE_LOSS = 7      /* the row kernel of spd_masked_token_loss */
+    SPD_PROFILE_LOSS = 7,     /* the row kernel of spd_masked_token_loss */
+    SPD_PROFILE_PAD = 8       /* the kernel of spd_pad_for_sequence_parallel */
 };
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel);
 
@@ -215,6 +217,25 @@ int spd_pack_tokens(const int32_t *tokens, const int32_t *doc_lens, int64_t num_
 int spd_unpack_data(const int32_t *input_ids, const int32_t *labels, const int32_t *cu_seqlens,
                     const int32_t *row_seg_ptr, int64_t rows, int micro_bsz, int seq_len, int32_t *out_ids,
                     int32_t *out_labels, spd_stream_t stream);
+
+/*
+ * pad_for_sequence_parallel (XTuner page "Sequence parallel training of
+ * extremely long sequences", section "Sequence parallel API", data pad and
+ * split): pad every row of an int32 tensor [rows][len] to padded = the
+ * smallest multiple of sp_size >= len, so the row splits evenly over the
+ * sequence-parallel ranks: dst int32 [rows][padded], dst[r][j] = src[r][j]
+ * for j < len; the added positions hold pad_value, or, with count_positions
+ * != 0, count 0, 1, 2, ... (position ids). The page names the tensors
+ * (input_ids, labels, position_ids, attention_mask) but not the values; the
+ * binding pads input_ids with 0 (the pad id), labels with -100 (the ignore
+ * index), position_ids by counting (the padding tail is its own segment, as
+ * in the packing rules) and attention_mask with 0. Returns
+ * SPD_ERR_INVALID_ARG for sp_size < 1, rows < 0, len < 0,
+ * rows * padded > 2^31 - 1, or a null / unaligned pointer with work to do;
+ * SPD_ERR_UNSUPPORTED or SPD_ERR_CUDA as above.
+ */
+int spd_pad_for_sequence_parallel(const int32_t *src, int32_t *dst, int64_t rows, int64_t len, int sp_size,
+                                  int32_t pad_value, int count_positions, spd_stream_t stream);
 
 /*
  * split_data_sequence_parallel (page "Data loading and flow", section

@@ -183,6 +183,34 @@ def unpack_data(packed_ids, packed_labels, cu_row, micro_bsz, seq_len):
     return out_ids, out_lab
 
 
+# Pad values of pad_for_sequence_parallel (XTuner page, "Sequence parallel API",
+# data pad and split): the page names the tensors (input_ids, labels,
+# position_ids, attention_mask) but not the values; read as the pad id 0 and
+# the ignore index -100 of the packing page, position ids that count 0, 1, 2, ...
+# over the added positions (the packing page's padding tail is a segment of its
+# own whose indexes count from 0), and attention mask 0 (padding attends to
+# nothing and is attended by nothing).
+SP_PAD = {"input_ids": ("value", PAD_ID), "labels": ("value", IGNORE_INDEX),
+          "position_ids": ("count", 0), "attention_mask": ("value", 0)}
+
+
+def sp_padded_length(n, sp_size):
+    """Smallest multiple of sp_size that is >= n."""
+    if sp_size < 1:
+        raise ValueError("sp_size must be >= 1")
+    return -(-n // sp_size) * sp_size
+
+
+def pad_for_sequence_parallel(seq, sp_size, kind):
+    """Pad one row of `kind` (a key of SP_PAD) so that its length divides by
+    sp_size; the original positions are kept as they are."""
+    mode, v = SP_PAD[kind]
+    n = len(seq)
+    extra = sp_padded_length(n, sp_size) - n
+    fill = [v] * extra if mode == "value" else list(range(extra))
+    return list(seq) + fill
+
+
 def split_sequence_parallel(seq, sp_size, rank):
     """section "Processing data", split_data_sequence_parallel: contiguous
     equal chunks of the sequence dimension, one per rank."""

@@ -181,7 +181,7 @@ int spd_debug_skip_arrive(int which)
 
 int spd_set_profile_events(void *begin_event, void *end_event, int kernel)
 {
-    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_LOSS) return SPD_ERR_INVALID_ARG;
+    if (kernel < SPD_PROFILE_NONE || kernel > SPD_PROFILE_PAD) return SPD_ERR_INVALID_ARG;
     ProfileHook &h = profile_hook();
     h.begin = static_cast<cudaEvent_t>(begin_event);
     h.end = static_cast<cudaEvent_t>(end_event);
@@ -323,6 +323,29 @@ int spd_unpack_data(const int32_t *input_ids, const int32_t *labels, const int32
     a.out_labels = out_labels;
     a.vec_out = aligned(out_ids, 16) && aligned(out_labels, 16);
     return cuda_rc(launch_unpack(a, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int spd_pad_for_sequence_parallel(const int32_t *src, int32_t *dst, int64_t rows, int64_t len, int sp_size,
+                                  int32_t pad_value, int count_positions, spd_stream_t stream)
+{
+    if (sp_size < 1 || rows < 0 || len < 0 || len > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    const int64_t padded = (len + sp_size - 1) / sp_size * sp_size;
+    if (rows * padded > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (rows == 0 || padded == 0) return SPD_OK;
+    if (!dst || !aligned(dst, 4) || (len > 0 && (!src || !aligned(src, 4)))) return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    PadArgs a = {};
+    a.src = src;
+    a.dst = dst;
+    a.rows = static_cast<int32_t>(rows);
+    a.len = static_cast<int32_t>(len);
+    a.padded = static_cast<int32_t>(padded);
+    a.value = pad_value;
+    a.count = count_positions ? 1 : 0;
+    a.vec = aligned(dst, 16) ? 1 : 0;
+    return cuda_rc(launch_pad(a, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const int32_t *src2, int64_t rows,

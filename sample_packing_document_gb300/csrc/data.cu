@@ -22,7 +22,10 @@ __global__ void __launch_bounds__(kThreads) unpack_kernel(UnpackArgs a)
     const int32_t plen = a.micro_bsz * a.seq_len;
     const int32_t total = a.rows * plen;
     const bool vec = a.vec_out && (a.seq_len & 3) == 0;   // a group of 4 never crosses an output row
-    for (int32_t x = (blockIdx.x * kThreads + threadIdx.x) * 4; x < total; x += gridDim.x * kThreads * 4) {
+    // 64-bit loop index: the step past the last group must not wrap (total < 2^31)
+    for (int64_t xl = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * 4; xl < total;
+         xl += static_cast<int64_t>(gridDim.x) * kThreads * 4) {
+        const int32_t x = static_cast<int32_t>(xl);
         int32_t id[4], lab[4];
         int32_t cur_key = -1, a0 = 0, n = 0;   // segment of the last output row looked up
 #pragma unroll
@@ -67,7 +70,10 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a)
     const int32_t chunk = a.len / a.sp_size;
     const int32_t total = a.rows * chunk;
     const int32_t off = a.rank * chunk;
-    for (int32_t x = (blockIdx.x * kThreads + threadIdx.x) * 4; x < total; x += gridDim.x * kThreads * 4) {
+    // 64-bit loop index: the step past the last group must not wrap (total < 2^31)
+    for (int64_t xl = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * 4; xl < total;
+         xl += static_cast<int64_t>(gridDim.x) * kThreads * 4) {
+        const int32_t x = static_cast<int32_t>(xl);
         const int32_t r = x / chunk, j = x - r * chunk;
         const int32_t src = r * a.len + off + j;
         for (int t = 0; t < a.n_tensors; ++t) {
@@ -79,6 +85,37 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a)
                     a.dst[t][x + k] = a.src[t][rr * a.len + off + jj];
                 }
             }
+        }
+    }
+}
+
+// dst[r][j] = src[r][j] (j < len), else the fill; four consecutive outputs per
+// thread (one 16-byte store when aligned: dst rows need not be, the group may
+// straddle two rows).
+__global__ void __launch_bounds__(kThreads) pad_kernel(PadArgs a)
+{
+    const int32_t total = a.rows * a.padded;
+    // 64-bit loop index: the step past the last group must not wrap (total < 2^31)
+    for (int64_t xl = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * 4; xl < total;
+         xl += static_cast<int64_t>(gridDim.x) * kThreads * 4) {
+        const int32_t x = static_cast<int32_t>(xl);
+        int32_t v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int32_t q = x + k;
+            if (q >= total) {
+                v[k] = 0;
+                continue;
+            }
+            const int32_t r = q / a.padded, j = q - r * a.padded;
+            v[k] = j < a.len ? a.src[static_cast<int64_t>(r) * a.len + j] : (a.count ? j - a.len : a.value);
+        }
+        if (a.vec && x + 4 <= total) {
+            *reinterpret_cast<int4 *>(a.dst + x) = make_int4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (x + k < total) a.dst[x + k] = v[k];
         }
     }
 }
@@ -101,6 +138,16 @@ cudaError_t launch_unpack(const UnpackArgs &a, int num_sms, cudaStream_t stream)
     prof_begin(kProfUnpack, stream);
     unpack_kernel<<<grid_for((total + 3) / 4, num_sms), kThreads, 0, stream>>>(a);
     prof_end(kProfUnpack, stream);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pad(const PadArgs &a, int num_sms, cudaStream_t stream)
+{
+    const int64_t total = static_cast<int64_t>(a.rows) * a.padded;
+    if (total == 0) return cudaSuccess;
+    prof_begin(kProfPad, stream);
+    pad_kernel<<<grid_for((total + 3) / 4, num_sms), kThreads, 0, stream>>>(a);
+    prof_end(kProfPad, stream);
     return cudaGetLastError();
 }
 

@@ -12,7 +12,7 @@ namespace spd {
 // Measurement hook (spd_set_profile_events): when `which` names a kernel,
 // its launcher records `begin` / `end` on the launch stream around that one
 // kernel. Per host thread.
-enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3, kProfUnpack = 4, kProfSplit = 5, kProfRope = 6, kProfLoss = 7 };
+enum { kProfNone = 0, kProfPackStream = 1, kProfAttnFwd = 2, kProfAttnBwd = 3, kProfUnpack = 4, kProfSplit = 5, kProfRope = 6, kProfLoss = 7, kProfPad = 8 };
 struct ProfileHook {
     cudaEvent_t begin = nullptr, end = nullptr;
     int which = kProfNone;
@@ -90,6 +90,17 @@ struct SplitArgs {
     int vec;                               // 1: 16-byte copies (aligned pointers, chunk % 4 == 0)
 };
 cudaError_t launch_split(const SplitArgs &a, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- sequence-parallel padding
+struct PadArgs {
+    const int32_t *src;                    // [rows][len]
+    int32_t *dst;                          // [rows][padded]
+    int32_t rows, len, padded;
+    int32_t value;                         // fill of the added positions ...
+    int count;                             // ... or 1: they count 0, 1, 2, ...
+    int vec;                               // 1: 16-byte stores (aligned dst)
+};
+cudaError_t launch_pad(const PadArgs &a, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- rotary position embedding
 struct RopeArgs {

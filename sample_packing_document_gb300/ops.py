@@ -39,6 +39,7 @@ SIGNATURES = {
                                            _P]),
     "spd_unpack_data": (_INT, [_P, _P, _P, _P, _I64, _INT, _INT, _P, _P, _P]),
     "spd_split_sequence_parallel": (_INT, [_P, _P, _P, _I64, _I64, _INT, _INT, _P, _P, _P, _P]),
+    "spd_pad_for_sequence_parallel": (_INT, [_P, _P, _I64, _I64, _INT, _I32, _INT, _P]),
     "spd_rope": (_INT, [_P, _P, _P, _I64, _INT, _INT, _INT, _F32, _INT, _P]),
     "spd_masked_token_loss": (_INT, [_P, _P, _I64, _I64, _P, _P, _P, _P, _F32, _P, _P]),
 }
@@ -105,7 +106,11 @@ def read_status(ws, stream=None):
 
 
 (PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD, PROFILE_UNPACK, PROFILE_SPLIT,
- PROFILE_ROPE, PROFILE_LOSS) = 0, 1, 2, 3, 4, 5, 6, 7
+ PROFILE_ROPE, PROFILE_LOSS, PROFILE_PAD) = 0, 1, 2, 3, 4, 5, 6, 7, 8
+
+# Pad of each tensor pad_for_sequence_parallel pads: (value, count): the pad id,
+# the ignore index, position ids counting 0, 1, 2, ... and attention mask 0.
+SP_PAD = {"input_ids": (0, False), "labels": (-100, False), "position_ids": (0, True), "attention_mask": (0, False)}
 
 
 def set_profile_events(begin, end, kernel):
@@ -216,6 +221,29 @@ def split_sequence_parallel(tensors, sp_size, rank, out=None, stream=None):
         src[0], src[1], src[2], int(rows), int(n), int(sp_size), int(rank), dst[0], dst[1], dst[2],
         _stream(stream)))
     return out
+
+
+def pad_for_sequence_parallel(sp_size, input_ids=None, labels=None, position_ids=None, attention_mask=None,
+                              stream=None):
+    """spd_pad_for_sequence_parallel on each given int32 CUDA tensor [rows, len]
+    (or [len]): padded to the smallest multiple of sp_size along the sequence
+    with the pad of its kind (SP_PAD). Returns the four results in order (None
+    for tensors not given)."""
+    out = []
+    for kind, x in (("input_ids", input_ids), ("labels", labels), ("position_ids", position_ids),
+                    ("attention_mask", attention_mask)):
+        if x is None:
+            out.append(None)
+            continue
+        _need_cuda(x)
+        rows, n = (1, x.shape[0]) if x.dim() == 1 else (x.shape[0], x.shape[1])
+        padded = -(-n // sp_size) * sp_size if sp_size >= 1 else n
+        y = torch.empty((padded,) if x.dim() == 1 else (rows, padded), dtype=torch.int32, device=x.device)
+        value, count = SP_PAD[kind]
+        _check("spd_pad_for_sequence_parallel", load().spd_pad_for_sequence_parallel(
+            _ptr(x), _ptr(y), int(rows), int(n), int(sp_size), int(value), int(count), _stream(stream)))
+        out.append(y)
+    return tuple(out)
 
 
 def rope(q, k, positions, rope_theta=None, inverse=False, stream=None):

@@ -61,6 +61,20 @@ def test_pack_num_segs_matches_the_oracle(lib):
         ops.pack_num_segs([3, 0, 2], 2, 8, True)
 
 
+def test_pad_for_sequence_parallel_host_checks(lib):
+    """Argument checks answered on the host, before any GPU work."""
+    import ctypes as C
+    from sample_packing_document_gb300 import ops
+    L = ops.load()
+    fake = C.c_void_p(4096)
+    assert L.spd_pad_for_sequence_parallel(fake, fake, 1, 10, 0, 0, 0, None) == -1      # sp_size < 1
+    assert L.spd_pad_for_sequence_parallel(fake, fake, -1, 10, 4, 0, 0, None) == -1     # rows < 0
+    assert L.spd_pad_for_sequence_parallel(fake, fake, 4, 2 ** 30, 3, 0, 0, None) == -1  # rows * padded > 2^31 - 1
+    assert L.spd_pad_for_sequence_parallel(fake, None, 1, 10, 4, 0, 0, None) == -1      # no output
+    assert L.spd_pad_for_sequence_parallel(fake, C.c_void_p(4098), 1, 10, 4, 0, 0, None) == -1   # unaligned
+    assert L.spd_pad_for_sequence_parallel(None, None, 0, 10, 4, 0, 0, None) == 0       # nothing to do
+
+
 def test_pack_rows_host_logic(lib):
     from sample_packing_document_gb300 import ops
     assert ops.pack_rows(4, 24, 2, 8, True) == (2, 8)        # the page's example: 2 rows

@@ -97,6 +97,45 @@ def test_split_random_matches_oracle(rows, length, sp):
             assert np.array_equal(g.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("rows,length,sp", [(1, 13, 8), (3, 24, 8), (5, 1001, 4), (2, 4093, 8), (7, 30, 1),
+                                             (1, 1, 5), (4, 0, 3), (2, 15, 16)])
+def test_pad_for_sequence_parallel_matches_oracle(rows, length, sp):
+    """Every tensor kind, ragged and already-divisible lengths, the empty row,
+    sp_size larger than the row; then the page's purpose: the padded rows split
+    evenly (split of the pad = split of the oracle's pad on every rank)."""
+    ops = _ops()
+    rng = np.random.default_rng(rows * 1000 + length + sp)
+    src = {k: rng.integers(-100, 50000, size=(rows, length)).astype(np.int32)
+           for k in ("input_ids", "labels", "position_ids", "attention_mask")}
+    got = ops.pad_for_sequence_parallel(sp, **{k: torch.tensor(v, device="cuda") for k, v in src.items()})
+    wants = []
+    for g, (k, x) in zip(got, src.items()):
+        want = np.array([P.pad_for_sequence_parallel(list(row), sp, k) for row in x], dtype=np.int32).reshape(rows, -(-length // sp) * sp)
+        assert np.array_equal(g.cpu().numpy(), want), k
+        wants.append(want)
+    if length > 0:
+        for r in range(sp):
+            parts = ops.split_sequence_parallel(list(got[:3]), sp, r)
+            for part, want in zip(parts, wants[:3]):
+                assert np.array_equal(part.cpu().numpy(),
+                                      np.array([P.split_sequence_parallel(list(row), sp, r) for row in want]))
+
+
+def test_pad_1d_and_unaligned_output():
+    """A [len] tensor, and an output view that is not 16-byte aligned (the
+    scalar store path)."""
+    ops = _ops()
+    x = torch.arange(1, 11, dtype=torch.int32, device="cuda")
+    (y,) = [t for t in ops.pad_for_sequence_parallel(4, labels=x) if t is not None]
+    assert y.cpu().tolist() == list(range(1, 11)) + [-100, -100]
+    lib = ops.load()
+    buf = torch.zeros(64, dtype=torch.int32, device="cuda")
+    rc = lib.spd_pad_for_sequence_parallel(ops._ptr(x), ops._ptr(buf[1:]), 1, 10, 4, 0, 1, ops._stream(None))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert buf[1:13].cpu().tolist() == list(range(1, 11)) + [0, 1] and int(buf[0]) == 0 and int(buf[13]) == 0
+
+
 def test_split_rejects_a_length_that_does_not_divide():
     ops = _ops()
     x = torch.zeros((2, 10), dtype=torch.int32, device="cuda")

@@ -71,6 +71,45 @@ def test_split_after_unpack_worked_example():
         assert [P.split_sequence_parallel(row, s["sp_size"], r) for row in g["unpacked_labels"]] == want["labels"]
 
 
+def test_pad_for_sequence_parallel_pins():
+    """No worked example on the page: pinned by what it states (the padded
+    length divides by the sequence-parallel size so the row splits evenly) and
+    by the packing page's own rules for the values read for the pad."""
+    import numpy as np
+    from oracle import loss as L
+    rng = np.random.default_rng(3)
+    for _ in range(40):
+        n, sp = int(rng.integers(1, 60)), int(rng.integers(1, 9))
+        seq = rng.integers(-100, 50000, size=n).tolist()
+        for kind in ("input_ids", "labels", "position_ids", "attention_mask"):
+            out = P.pad_for_sequence_parallel(seq, sp, kind)
+            assert len(out) % sp == 0 and len(out) - len(seq) < sp and out[:n] == seq
+            if n % sp == 0:
+                assert out == seq
+            # the page's purpose: the padded row splits into equal chunks that rebuild it
+            chunks = [P.split_sequence_parallel(out, sp, r) for r in range(sp)]
+            assert all(len(c) == len(out) // sp for c in chunks) and sum(chunks, []) == out
+    # labels: the added tokens are ignored by the masked loss (same loss, same count)
+    logits_rng = np.random.default_rng(4)
+    labels = logits_rng.integers(0, 11, size=13).tolist()
+    labels[5] = P.IGNORE_INDEX
+    padded = P.pad_for_sequence_parallel(labels, 8, "labels")
+    lg = logits_rng.normal(size=(len(padded), 11))
+    a = L.masked_loss(lg[:13], np.array(labels))
+    b = L.masked_loss(lg, np.array(padded))
+    assert a[0] == b[0] and a[1] == b[1]
+    # input ids: the pad id of the packing rules
+    assert P.pad_for_sequence_parallel([7, 8, 9], 4, "input_ids") == [7, 8, 9, P.PAD_ID]
+    # position ids: the added positions are indexed like a padding segment of
+    # their own (row_indexes of the row with one more boundary at the old end)
+    g = GOLDEN["build_pack"]
+    b = P.pack_batch(g["docs"], g["micro_bsz"], g["seq_len"], True)
+    idx, cu = b["indexes"][1], b["cu_seqlens"][1]
+    for sp in (3, 5, 7):
+        padded = P.pad_for_sequence_parallel(idx, sp, "position_ids")
+        assert padded == P.row_indexes(cu + [len(padded)])[:len(padded)]
+
+
 def test_flat_layout_worked_example():
     g = GOLDEN["build_pack"]
     f = P.pack_flat(g["docs"], g["micro_bsz"], g["seq_len"], True)
