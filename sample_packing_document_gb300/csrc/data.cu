@@ -76,11 +76,17 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a)
         const int32_t x = static_cast<int32_t>(xl);
         const int32_t r = x / chunk, j = x - r * chunk;
         const int32_t src = r * a.len + off + j;
-        for (int t = 0; t < a.n_tensors; ++t) {
+        // unrolled over the (at most three) tensors so that the pointer arrays are
+        // indexed with constants and stay in the parameter space
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            if (t >= a.n_tensors) break;
             if (a.vec && x + 4 <= total) {   // chunk % 4 == 0: the group stays in one row
                 *reinterpret_cast<int4 *>(a.dst[t] + x) = *reinterpret_cast<const int4 *>(a.src[t] + src);
             } else {
-                for (int k = 0; k < 4 && x + k < total; ++k) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (x + k >= total) break;
                     const int32_t rr = (x + k) / chunk, jj = (x + k) - rr * chunk;
                     a.dst[t][x + k] = a.src[t][rr * a.len + off + jj];
                 }
