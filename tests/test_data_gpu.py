@@ -121,6 +121,21 @@ def test_pad_for_sequence_parallel_matches_oracle(rows, length, sp):
                                       np.array([P.split_sequence_parallel(list(row), sp, r) for row in want]))
 
 
+def test_pad_full_size_row():
+    """The timed case: one 1048573-token row padded to sp_size 8 (1048576), every
+    tensor kind, compared in full with the oracle."""
+    ops = _ops()
+    T, sp = (1 << 20) - 3, 8
+    rng = np.random.default_rng(11)
+    src = rng.integers(-100, 50000, size=(1, T)).astype(np.int32)
+    x = torch.tensor(src, device="cuda")
+    got = ops.pad_for_sequence_parallel(sp, input_ids=x, labels=x, position_ids=x, attention_mask=x)
+    for g, kind in zip(got, ("input_ids", "labels", "position_ids", "attention_mask")):
+        want = np.array(P.pad_for_sequence_parallel(src[0].tolist(), sp, kind), dtype=np.int32)
+        assert g.shape == (1, 1 << 20)
+        assert np.array_equal(g.cpu().numpy()[0], want), kind
+
+
 def test_pad_1d_and_unaligned_output():
     """A [len] tensor, and an output view that is not 16-byte aligned (the
     scalar store path)."""
