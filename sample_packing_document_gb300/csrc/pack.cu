@@ -13,11 +13,13 @@
 //   pack_scan_kernel    one CTA: prefix sums over the document lengths, the
 //                       document -> output position map, cu_seqlens,
 //                       row_seg_ptr, max_seqlen, num_segs. Work ~ num_docs.
-//   pack_stream_kernel  all SMs: the token stream, 16-byte vector stores of
+//   pack_packed_stream_kernel (build_pack) / unpack_stream_kernel (build_unpack)
+//                       all SMs: the token stream, 16-byte vector stores of
 //                       input_ids / labels / indexes. Work ~ output positions.
 // The stream kernel is a programmatic dependent launch: in build_pack mode it
-// copies input_ids (which needs no document boundaries) while the scan runs,
-// then waits for the scan's results before labels and indexes.
+// loads its tokens and stores input_ids (which needs no document boundaries)
+// while the scan runs, then waits for the scan's results before labels and
+// indexes.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -26,6 +28,7 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 constexpr int kScanItems = 4;  // documents per thread per pass
+constexpr int kScanSmemDocs = 8192;   // build_pack: document offsets staged in shared memory up to this count
 constexpr int kStreamThreads = 256;
 constexpr int kStreamIters = 4;
 constexpr int kChunk = kStreamThreads * 4 * kStreamIters;  // positions per CTA
@@ -147,13 +150,22 @@ __global__ void __launch_bounds__(kScanThreads) pack_scan_kernel(PackArgs a, int
 
     int num_segs;
     if (a.packed) {
+        // The document offsets are read many times below (every row's binary
+        // search among them): from shared memory when they fit.
+        __shared__ int32_t s_in[kScanSmemDocs];
+        const bool in_smem = nd + 1 <= kScanSmemDocs;
+        if (in_smem) {
+            for (int d = tid; d <= nd; d += kScanThreads) s_in[d] = a.doc_in[d];
+            __syncthreads();
+        }
+        const int32_t *din = in_smem ? s_in : a.doc_in;
         // Segment boundaries are the union of document starts, row starts and
         // the padding start. A document start that falls on a row start is
         // the same boundary; count those ("aligned") so ranks stay exact.
         long long carry_al = 0;
         for (int base = 0; base < nd; base += kScanThreads) {
             int d = base + tid;
-            int flag = (d >= 1 && d < nd && (a.doc_in[d] % plen) == 0) ? 1 : 0;
+            int flag = (d >= 1 && d < nd && (din[d] % plen) == 0) ? 1 : 0;
             long long tot;
             long long e = block_excl_scan(flag, &tot, sh) + carry_al;
             if (d < nd) aux[d] = static_cast<int32_t>(e);  // aligned starts before d
@@ -165,7 +177,7 @@ __global__ void __launch_bounds__(kScanThreads) pack_scan_kernel(PackArgs a, int
         const int pad = (total % plen) != 0;
         num_segs = a.rows == 0 ? 0 : static_cast<int>(a.rows + nd - 1 - aux[nd] + pad);
         for (int d = tid; d < nd; d += kScanThreads) {
-            long long s = a.doc_in[d];
+            long long s = din[d];
             a.doc_out[d] = static_cast<int32_t>(s);
             if (d >= 1 && (s % plen) != 0) {
                 long long rank = (s - 1) / plen + d - aux[d];
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(kScanThreads) pack_scan_kernel(PackArgs a, int
         for (int r = tid; r <= a.rows; r += kScanThreads) {
             long long rank = 0;
             if (r > 0) {
-                int ds = lower_bound(a.doc_in, 0, nd, r * plen);
+                int ds = lower_bound(din, 0, nd, r * plen);
                 rank = r + ds - 1 - aux[ds] + ((r == a.rows && pad) ? 1 : 0);
             }
             a.cu_seqlens[rank] = static_cast<int32_t>(r * plen);
@@ -226,101 +238,60 @@ __global__ void __launch_bounds__(kScanThreads) pack_scan_kernel(PackArgs a, int
     }
 }
 
-// Per output position: id, label, index. `d_hint` is a document index at or
-// before the one holding p (build_pack) and is advanced in place.
-template <bool kPacked>
-__device__ __forceinline__ void one_position(const PackArgs &a, long long p, int &d, int d_end,
-                                             int32_t &id, int32_t &lab, int32_t &idx)
+// build_unpack, per output position: id, label, index. Row r holds documents
+// r * micro_bsz .. +micro_bsz - 1, each truncated to SEQ_LEN, then padding.
+__device__ __forceinline__ void unpack_position(const PackArgs &a, long long p, int32_t &id, int32_t &lab,
+                                                int32_t &idx)
 {
     const long long plen = a.plen;
-    if (kPacked) {
-        const long long total = a.num_tokens;
-        if (p >= total) {
-            id = 0;
-            lab = -100;
-            idx = static_cast<int32_t>(p - total);
-            return;
-        }
-        while (d + 1 < d_end && a.doc_out[d + 1] <= p) ++d;
-        const long long start = a.doc_out[d], end = a.doc_out[d + 1];
-        id = a.tokens[p];
-        lab = (p + 1 < end) ? a.tokens[p + 1] : -100;
-        const long long row_start = (p / plen) * plen;
-        idx = static_cast<int32_t>(p - (start > row_start ? start : row_start));
+    const long long r = p / plen;
+    const int d0 = static_cast<int>(r * a.micro_bsz);
+    const int d1 = min(a.num_docs, d0 + a.micro_bsz);
+    const int dd = last_le(a.doc_out, d0, d1, p);
+    const long long start = a.doc_out[dd];
+    const int keep = a.doc_keep[dd];
+    const long long t = p - start;
+    if (t < keep) {
+        const long long src = static_cast<long long>(a.doc_in[dd]) + t;
+        id = a.tokens[src];
+        lab = (t + 1 < keep) ? a.tokens[src + 1] : -100;
+        idx = static_cast<int32_t>(t);
     } else {
-        const long long r = p / plen;
-        const int d0 = static_cast<int>(r * a.micro_bsz);
-        const int d1 = min(a.num_docs, d0 + a.micro_bsz);
-        const int dd = last_le(a.doc_out, d0, d1, p);
-        const long long start = a.doc_out[dd];
-        const int keep = a.doc_keep[dd];
-        const long long t = p - start;
-        if (t < keep) {
-            const long long src = static_cast<long long>(a.doc_in[dd]) + t;
-            id = a.tokens[src];
-            lab = (t + 1 < keep) ? a.tokens[src + 1] : -100;
-            idx = static_cast<int32_t>(t);
-        } else {
-            id = 0;
-            lab = -100;
-            idx = static_cast<int32_t>(t - keep);
-        }
+        id = 0;
+        lab = -100;
+        idx = static_cast<int32_t>(t - keep);
     }
 }
 
-template <bool kPacked>
-__global__ void __launch_bounds__(kStreamThreads) pack_stream_kernel(PackArgs a)
+__global__ void __launch_bounds__(kStreamThreads) unpack_stream_kernel(PackArgs a)
 {
     const long long npos = static_cast<long long>(a.rows) * a.plen;
     const long long P0 = static_cast<long long>(blockIdx.x) * kChunk;
     const long long P1 = min(npos, P0 + kChunk);
-
-    if (kPacked) {
-        // input_ids needs no document boundaries: copy it while the scan runs.
-        for (int it = 0; it < kStreamIters; ++it) {
-            long long p = P0 + (static_cast<long long>(it) * kStreamThreads + threadIdx.x) * 4;
-            if (p >= P1) break;
-            if (a.vec_out && a.vec_in && p + 4 <= a.num_tokens) {
-                *reinterpret_cast<int4 *>(a.input_ids + p) =
-                    *reinterpret_cast<const int4 *>(a.tokens + p);
-            } else {
-                for (int k = 0; k < 4 && p + k < P1; ++k)
-                    a.input_ids[p + k] = p + k < a.num_tokens ? a.tokens[p + k] : 0;
-            }
-        }
-    }
     pdl_wait();
     if (*reinterpret_cast<volatile int *>(a.status) != 0) return;
-
-    __shared__ int d_lo_s, d_hi_s;
-    if (kPacked) {
-        if (threadIdx.x == 0) {
-            long long last_tok = a.num_tokens - 1;
-            long long q0 = P0 < last_tok ? P0 : last_tok;
-            long long q1 = (P1 - 1) < last_tok ? (P1 - 1) : last_tok;
-            d_lo_s = a.num_docs > 0 ? last_le(a.doc_out, 0, a.num_docs, q0) : 0;
-            d_hi_s = a.num_docs > 0 ? last_le(a.doc_out, 0, a.num_docs, q1) + 1 : 0;
-        }
-        __syncthreads();
-    }
     for (int it = 0; it < kStreamIters; ++it) {
         long long p = P0 + (static_cast<long long>(it) * kStreamThreads + threadIdx.x) * 4;
         if (p >= P1) break;
-        int d = 0;
-        if (kPacked && p < a.num_tokens) d = last_le(a.doc_out, d_lo_s, d_hi_s, p);
         int32_t id[4], lab[4], idx[4];
         const int n = static_cast<int>(min(4LL, P1 - p));
-        for (int k = 0; k < n; ++k)
-            one_position<kPacked>(a, p + k, d, d_hi_s, id[k], lab[k], idx[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (k < n) unpack_position(a, p + k, id[k], lab[k], idx[k]);
+            else id[k] = lab[k] = idx[k] = 0;
+        }
         if (a.vec_out && n == 4) {
-            if (!kPacked) *reinterpret_cast<int4 *>(a.input_ids + p) = make_int4(id[0], id[1], id[2], id[3]);
+            *reinterpret_cast<int4 *>(a.input_ids + p) = make_int4(id[0], id[1], id[2], id[3]);
             *reinterpret_cast<int4 *>(a.labels + p) = make_int4(lab[0], lab[1], lab[2], lab[3]);
             *reinterpret_cast<int4 *>(a.indexes + p) = make_int4(idx[0], idx[1], idx[2], idx[3]);
         } else {
-            for (int k = 0; k < n; ++k) {
-                if (!kPacked) a.input_ids[p + k] = id[k];
-                a.labels[p + k] = lab[k];
-                a.indexes[p + k] = idx[k];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (k < n) {
+                    a.input_ids[p + k] = id[k];
+                    a.labels[p + k] = lab[k];
+                    a.indexes[p + k] = idx[k];
+                }
             }
         }
     }
@@ -375,6 +346,130 @@ __device__ __forceinline__ int last_le_smem(const int32_t *a, int n, long long x
         else hi = mid;
     }
     return lo;
+}
+
+__device__ __forceinline__ int32_t int4_at(const int4 &v, int k)
+{
+    return k == 0 ? v.x : k == 1 ? v.y : k == 2 ? v.z : v.w;
+}
+
+// build_pack token stream (more documents or rows than the fused path takes):
+// kChunk consecutive output positions per CTA, four per thread per iteration.
+// The chunk's tokens are loaded once into registers and input_ids (which needs
+// no document boundaries) is stored while the scan kernel may still run. After
+// the scan, the CTA finds the document holding its first position with a
+// block-wide search (256 sampled starts per round, one barrier each) and
+// stages the starts of the documents its chunk overlaps in shared memory;
+// labels and indexes then need no global lookups.
+constexpr int kWin = 1024;   // document starts staged per CTA
+
+__global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(PackArgs a)
+{
+    __shared__ int32_t s_doc[kWin];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int total = a.num_tokens, nd = a.num_docs, plen = a.plen;
+    const int npos = a.rows * plen;   // rows * plen <= 2^31 - 1 is checked on the host
+    const int P0 = static_cast<int>(blockIdx.x) * kChunk;
+    const int P1 = min(npos, P0 + kChunk);
+
+    int4 tk[kStreamIters];
+    int32_t nx[kStreamIters];   // the token after each group of four (its last label)
+#pragma unroll
+    for (int it = 0; it < kStreamIters; ++it) {
+        const int p = P0 + (it * kStreamThreads + tid) * 4;
+        if (a.vec_in && p + 4 <= total) {
+            tk[it] = __ldg(reinterpret_cast<const int4 *>(a.tokens + p));
+        } else {
+            tk[it].x = p < total ? __ldg(a.tokens + p) : 0;
+            tk[it].y = p + 1 < total ? __ldg(a.tokens + p + 1) : 0;
+            tk[it].z = p + 2 < total ? __ldg(a.tokens + p + 2) : 0;
+            tk[it].w = p + 3 < total ? __ldg(a.tokens + p + 3) : 0;
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < kStreamIters; ++it) {
+        const int p = P0 + (it * kStreamThreads + tid) * 4;
+        int32_t v = __shfl_down_sync(0xffffffffu, tk[it].x, 1);
+        if (lane == 31) v = p + 4 < total ? __ldg(a.tokens + p + 4) : 0;
+        nx[it] = v;
+        if (p >= P1) continue;
+        if (a.vec_out && p + 4 <= P1) {
+            *reinterpret_cast<int4 *>(a.input_ids + p) = tk[it];
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (p + k < P1) a.input_ids[p + k] = int4_at(tk[it], k);
+        }
+    }
+    pdl_wait();
+    if (*reinterpret_cast<volatile int *>(a.status) != 0) return;
+
+    // The document holding position P0 (chunks wholly in the padding need none):
+    // doc_out[lo] <= P0 < doc_out[hi] throughout, the range shrinking 256-fold
+    // per round.
+    int d_lo = 0, W = 0;
+    bool staged = false;
+    if (P0 < total) {
+        int lo = 0, hi = nd;
+        while (hi - lo > 1) {
+            const int step = (hi - lo + kStreamThreads - 1) / kStreamThreads;
+            const int idx = lo + tid * step;
+            const bool le = idx < hi && a.doc_out[idx] <= P0;
+            const int cnt = __syncthreads_count(le);   // >= 1: doc_out[lo] <= P0
+            lo += (cnt - 1) * step;
+            hi = min(hi, lo + step);
+        }
+        d_lo = lo;
+        W = min(kWin, nd + 1 - d_lo);   // doc_out[nd] = num_tokens ends the last document
+        for (int i = tid; i < W; i += kStreamThreads) s_doc[i] = a.doc_out[d_lo + i];
+        __syncthreads();
+        // staged when the window reaches past the chunk's last token
+        staged = s_doc[W - 1] > min(P1, total) - 1;
+    }
+
+#pragma unroll
+    for (int it = 0; it < kStreamIters; ++it) {
+        const int p = P0 + (it * kStreamThreads + tid) * 4;
+        if (p >= P1) break;
+        int32_t lab[4], idx[4];
+        int d = 0;
+        if (p < total) d = staged ? last_le_smem(s_doc, W, p) : last_le(a.doc_out, d_lo, nd, p) - d_lo;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q = p + k;
+            if (q >= total) {   // the padding segment starts at num_tokens
+                lab[k] = -100;
+                idx[k] = q - total;
+                continue;
+            }
+            int start, end;
+            if (staged) {
+                while (s_doc[d + 1] <= q) ++d;   // q < s_doc[W - 1]
+                start = s_doc[d];
+                end = s_doc[d + 1];
+            } else {
+                while (a.doc_out[d_lo + d + 1] <= q) ++d;   // q < doc_out[nd]
+                start = a.doc_out[d_lo + d];
+                end = a.doc_out[d_lo + d + 1];
+            }
+            const int next = k < 3 ? int4_at(tk[it], k + 1) : nx[it];
+            lab[k] = q + 1 < end ? next : -100;
+            const int row_start = q - q % plen;
+            idx[k] = q - (start > row_start ? start : row_start);
+        }
+        if (a.vec_out && p + 4 <= P1) {
+            *reinterpret_cast<int4 *>(a.labels + p) = make_int4(lab[0], lab[1], lab[2], lab[3]);
+            *reinterpret_cast<int4 *>(a.indexes + p) = make_int4(idx[0], idx[1], idx[2], idx[3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (p + k < P1) {
+                    a.labels[p + k] = lab[k];
+                    a.indexes[p + k] = idx[k];
+                }
+            }
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kFusedThreads) pack_fused_kernel(PackArgs a)
@@ -576,8 +671,8 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     prof_begin(kProfPackStream, stream);
-    e = a.packed ? cudaLaunchKernelEx(&cfg, pack_stream_kernel<true>, a)
-                 : cudaLaunchKernelEx(&cfg, pack_stream_kernel<false>, a);
+    e = a.packed ? cudaLaunchKernelEx(&cfg, pack_packed_stream_kernel, a)
+                 : cudaLaunchKernelEx(&cfg, unpack_stream_kernel, a);
     prof_end(kProfPackStream, stream);
     return e;
 }

@@ -124,6 +124,74 @@ def test_unaligned_outputs_take_scalar_path(ops):
     np.testing.assert_array_equal(out["indexes"].cpu().numpy(), ref["indexes"])
 
 
+def test_random_two_launch_cases(ops):
+    """Random build_pack cases past the fused path's limits (more than 1024
+    documents or more than 512 rows): row starts on and inside documents,
+    documents longer than a row, padding, both kernel lookup paths."""
+    rng = np.random.default_rng(31)
+    for _ in range(40):
+        nd = int(rng.integers(1025, 2600)) if rng.random() < 0.7 else int(rng.integers(1, 200))
+        mb, sl = int(rng.integers(1, 4)), int(rng.integers(1, 40))
+        plen = mb * sl
+        hi = int(rng.choice([3, 3 * plen + 1, 600]))
+        lens = rng.integers(1, max(2, hi), size=nd).astype(np.int32)
+        toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+        ref = OA.pack(toks, lens, mb, sl, True)
+        if nd <= 1024 and ref["rows"] <= 512:
+            continue
+        st, g = _gpu_pack(ops, toks, lens, mb, sl, True)
+        assert st == 0
+        _assert_same(g, ref)
+
+
+@pytest.mark.parametrize("case", ["long_docs_16_rows", "tiny_docs_window_overflow", "many_rows_few_docs",
+                                  "unaligned_many_docs"])
+def test_two_launch_build_pack(ops, case):
+    """build_pack through the scan and token-stream launches (more than 1024
+    documents or 512 rows): documents spanning many 4096-position chunks, chunks
+    overlapping more documents than the 1024 starts a CTA stages (the global
+    lookup path), many rows, and unaligned tokens / outputs (scalar paths)."""
+    rng = np.random.default_rng({"long_docs_16_rows": 21, "tiny_docs_window_overflow": 22,
+                                 "many_rows_few_docs": 23, "unaligned_many_docs": 24}[case])
+    if case == "long_docs_16_rows":
+        from sample_packing_document_gb300 import workloads as W
+        w = W.WORKLOADS["c5"]
+        lens, toks = W.documents(w)
+        lens, toks = np.tile(np.asarray(lens, np.int32), 16), np.tile(np.asarray(toks, np.int32), 16)
+        mb, sl = w.micro_bsz, w.seq_len
+    elif case == "tiny_docs_window_overflow":
+        lens = rng.integers(1, 3, size=30000).astype(np.int32)      # ~2700 documents per 4096 positions
+        toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+        mb, sl = 1, 10000
+    elif case == "many_rows_few_docs":
+        lens = rng.integers(1, 200, size=300).astype(np.int32)
+        toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+        mb, sl = 2, 4                                               # > 512 rows of 8
+    else:
+        lens = rng.integers(1, 700, size=3000).astype(np.int32)
+        toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+        mb, sl = 3, 5000
+    ref = OA.pack(toks, lens, mb, sl, True)
+    if case != "unaligned_many_docs":
+        st, g = _gpu_pack(ops, toks, lens, mb, sl, True)
+        assert st == 0
+        _assert_same(g, ref)
+        return
+    n = ref["rows"] * mb * sl
+    base = torch.zeros(3 * n + 8, dtype=torch.int32, device="cuda")
+    out = ops.alloc_pack_outputs(len(lens), len(toks), mb, sl, True)
+    out["input_ids"], out["labels"], out["indexes"] = base[1:1 + n], base[2 + n:2 + 2 * n], base[3 + 2 * n:3 + 3 * n]
+    tb = torch.zeros(len(toks) + 1, dtype=torch.int32, device="cuda")
+    tb[1:] = torch.tensor(toks, device="cuda")
+    ops.pack_tokens(tb[1:], torch.tensor(lens, device="cuda"), mb, sl, True, out=out)
+    assert ops.read_status(out["ws"]) == 0
+    np.testing.assert_array_equal(out["input_ids"].cpu().numpy(), ref["input_ids"])
+    np.testing.assert_array_equal(out["labels"].cpu().numpy(), ref["labels"])
+    np.testing.assert_array_equal(out["indexes"].cpu().numpy(), ref["indexes"])
+    ns = int(out["num_segs"].item())
+    np.testing.assert_array_equal(out["cu_seqlens"][:ns + 1].cpu().numpy(), ref["cu_seqlens"])
+
+
 def test_bad_doc_lengths_set_status(ops):
     toks = torch.arange(1, 11, dtype=torch.int32, device="cuda")
     st, _ = _gpu_pack(ops, toks.cpu().numpy(), [4, 0, 6], 2, 4, True)
