@@ -10,7 +10,8 @@
 //
 // Three launches:
 //   bwd_pre_kernel   D_i = rowsum(dO * O) (fp32) and zeroes the fp32 dQ
-//                    accumulator, laid out [Hq][d / 32][T][32].
+//                    accumulator, laid out [Hq][d / 32][T][32]; runs beside the
+//                    tile schedule (programmatic dependent launch).
 //   attn_bwd_kernel  one CTA per (128-row kv tile, kv head): K, V stay in shared
 //                    memory; the CTA walks every (q head of the group, q tile
 //                    from the diagonal to the segment end). Per step, five
@@ -142,6 +143,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t *__restrict
     for (long long x = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; x < n4;
          x += static_cast<long long>(gridDim.x) * blockDim.x)
         z[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // Launched as a programmatic dependent of the tile schedule, which it does
+    // not read: it runs beside it, and does not complete before it, so the main
+    // kernel (a plain launch after this one) sees the finished schedule.
+    pdl_wait();
 }
 
 // ------------------------------------------------------------------ dq convert
@@ -726,8 +731,16 @@ cudaError_t launch_bwd_d(const AttnBwdArgs &a, int64_t max_units, cudaStream_t s
         long long blocks = (rows * 8 + 255) / 256;
         if (blocks > 152 * 16) blocks = 152 * 16;
         if (blocks < 1) blocks = 1;
-        bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a.out, a.dout, a.delta, a.dq_acc, T, a.Hq);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_pre_kernel<D>, a.out, a.dout, a.delta, a.dq_acc, T, a.Hq);
         if (e != cudaSuccess) return e;
     }
     const size_t smem = sizeof(BwdSmem<D>);

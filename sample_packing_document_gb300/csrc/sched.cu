@@ -55,6 +55,10 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
                                                             int *status, int32_t *count, Tile *tiles,
                                                             int32_t *tile_off)
 {
+    // The backward's preprocessing kernel depends on nothing computed here: let
+    // it start at once (programmatic dependent launch; it waits for this grid
+    // before it completes). No effect on kernels launched without the attribute.
+    pdl_launch_dependents();
     __shared__ int bins[kCostCap + 1];
     __shared__ long long sh[33];
     __shared__ int bad_s;
