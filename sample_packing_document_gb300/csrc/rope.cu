@@ -50,23 +50,37 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(const __grid_constant__ 
             uint16_t *base = which ? a.k : a.q;
             const int H = which ? a.Hkv : a.Hq;
             if (!base) continue;
-            for (int h = 0; h < H; ++h) {
-                uint16_t *row = base + (static_cast<size_t>(tok) * H + h) * a.d;
-                uint4 *plo = reinterpret_cast<uint4 *>(row + g * 8);
-                uint4 *phi = reinterpret_cast<uint4 *>(row + a.d / 2 + g * 8);
-                const uint4 lo4 = *plo, hi4 = *phi;
-                const uint32_t lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
-                uint32_t olo[4], ohi[4];
+            // four heads at a time: all eight loads are issued before the first
+            // store, so a thread keeps 128 bytes in flight
+            constexpr int kHeads = 4;
+            for (int h0 = 0; h0 < H; h0 += kHeads) {
+                uint4 lo4[kHeads], hi4[kHeads];
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float x0 = bf_lo(lo[w]), x1 = bf_hi(lo[w]);     // channels j, j + 1
-                    const float y0 = bf_lo(hi[w]), y1 = bf_hi(hi[w]);     // channels j + d/2, j + 1 + d/2
-                    const int e0 = 2 * w, e1 = 2 * w + 1;
-                    olo[w] = pack_bf16x2(x0 * c[e0] - y0 * s[e0], x1 * c[e1] - y1 * s[e1]);
-                    ohi[w] = pack_bf16x2(y0 * c[e0] + x0 * s[e0], y1 * c[e1] + x1 * s[e1]);
+                for (int u = 0; u < kHeads; ++u) {
+                    if (h0 + u < H) {
+                        const uint16_t *row = base + (static_cast<size_t>(tok) * H + h0 + u) * a.d;
+                        lo4[u] = *reinterpret_cast<const uint4 *>(row + g * 8);
+                        hi4[u] = *reinterpret_cast<const uint4 *>(row + a.d / 2 + g * 8);
+                    }
                 }
-                *plo = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-                *phi = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+#pragma unroll
+                for (int u = 0; u < kHeads; ++u) {
+                    if (h0 + u >= H) break;
+                    const uint32_t lo[4] = {lo4[u].x, lo4[u].y, lo4[u].z, lo4[u].w};
+                    const uint32_t hi[4] = {hi4[u].x, hi4[u].y, hi4[u].z, hi4[u].w};
+                    uint32_t olo[4], ohi[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const float x0 = bf_lo(lo[w]), x1 = bf_hi(lo[w]);     // channels j, j + 1
+                        const float y0 = bf_lo(hi[w]), y1 = bf_hi(hi[w]);     // channels j + d/2, j + 1 + d/2
+                        const int e0 = 2 * w, e1 = 2 * w + 1;
+                        olo[w] = pack_bf16x2(x0 * c[e0] - y0 * s[e0], x1 * c[e1] - y1 * s[e1]);
+                        ohi[w] = pack_bf16x2(y0 * c[e0] + x0 * s[e0], y1 * c[e1] + x1 * s[e1]);
+                    }
+                    uint16_t *row = base + (static_cast<size_t>(tok) * H + h0 + u) * a.d;
+                    *reinterpret_cast<uint4 *>(row + g * 8) = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+                    *reinterpret_cast<uint4 *>(row + a.d / 2 + g * 8) = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+                }
             }
         }
     }
