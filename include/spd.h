@@ -132,8 +132,9 @@ int spd_read_status(const void *ws, spd_stream_t stream, int *device_status);
  *   use_packed_dataset == 0 (build_unpack): rows = ceil(num_docs / micro_bsz),
  *   with plen = micro_bsz * seq_len. *max_segs bounds num_segs: size
  *   cu_seqlens with max_segs + 1 entries. Returns SPD_ERR_INVALID_ARG if a
- *   size is <= 0 (num_docs / num_tokens may be 0) or rows * plen does not fit
- *   in int32.
+ *   size is <= 0 (num_docs / num_tokens may be 0) or rows * plen exceeds
+ *   2^31 - 65537 (positions are 32-bit in the kernels, which step up to one
+ *   chunk past the last position before their bounds checks).
  */
 int spd_pack_rows(int64_t num_docs, int64_t num_tokens, int micro_bsz, int seq_len,
                   int use_packed_dataset, int64_t *rows, int64_t *max_segs);
@@ -210,7 +211,7 @@ int spd_pack_tokens(const int32_t *tokens, const int32_t *doc_lens, int64_t num_
  *   row_seg_ptr int32 [rows + 1].
  * Outputs (device): out_ids, out_labels int32 [rows][micro_bsz][seq_len].
  * rows == 0 is a no-op. Returns SPD_ERR_INVALID_ARG (micro_bsz or seq_len < 1,
- * rows < 0, rows * micro_bsz * seq_len > 2^31 - 1, a null or unaligned
+ * rows < 0, rows * micro_bsz * seq_len > 2^31 - 65537, a null or unaligned
  * pointer), SPD_ERR_UNSUPPORTED (not an sm_103 GPU) or SPD_ERR_CUDA. No
  * workspace: the segment offsets are trusted as spd_pack_tokens produced them.
  */
@@ -231,7 +232,7 @@ int spd_unpack_data(const int32_t *input_ids, const int32_t *labels, const int32
  * index), position_ids by counting (the padding tail is its own segment, as
  * in the packing rules) and attention_mask with 0. Returns
  * SPD_ERR_INVALID_ARG for sp_size < 1, rows < 0, len < 0,
- * rows * padded > 2^31 - 1, or a null / unaligned pointer with work to do;
+ * rows * padded > 2^31 - 65537, or a null / unaligned pointer with work to do;
  * SPD_ERR_UNSUPPORTED or SPD_ERR_CUDA as above.
  */
 int spd_pad_for_sequence_parallel(const int32_t *src, int32_t *dst, int64_t rows, int64_t len, int sp_size,
@@ -247,7 +248,7 @@ int spd_pad_for_sequence_parallel(const int32_t *src, int32_t *dst, int64_t rows
  * unused slots are NULL (src_i and dst_i together). Returns
  * SPD_ERR_INVALID_ARG if len % sp_size != 0 (the sequence must be padded
  * first), sp_size < 1, rank outside [0, sp_size), rows < 0, len < 0,
- * rows * len > 2^31 - 1, or a pointer is unaligned / unpaired;
+ * rows * len > 2^31 - 65537, or a pointer is unaligned / unpaired;
  * SPD_ERR_UNSUPPORTED or SPD_ERR_CUDA as above.
  */
 int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const int32_t *src2, int64_t rows,
@@ -329,8 +330,8 @@ size_t spd_attn_workspace_size(int64_t total_tokens, int32_t num_segs, int Hq, i
  *   cu_seqlens int32 [num_segs + 1], 0 = c0 < c1 < ... < c_num_segs =
  *   total_tokens (checked on the GPU: SPD_ERR_BAD_SEQLENS);
  *   max_seqlen (host) bounds the longest segment (a hint; <= 0 = unknown).
- * head_dim is 64 or 128; Hq % Hkv == 0; softmax_scale <= 0 means
- * 1 / sqrt(head_dim).
+ * head_dim is 64 or 128; Hq % Hkv == 0; total_tokens and Hq * total_tokens
+ * at most 2^31 - 65537; softmax_scale <= 0 means 1 / sqrt(head_dim).
  * Outputs (device): out bf16 [total_tokens, Hq, head_dim]; lse fp32
  *   [Hq, total_tokens] (natural log).
  */

@@ -108,9 +108,9 @@ int check_attn_shape(int64_t T, int32_t num_segs, int Hq, int Hkv, int D)
 {
     if (D != 64 && D != 128) return SPD_ERR_UNSUPPORTED;
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return SPD_ERR_INVALID_ARG;
-    if (T < 0 || T > 0x7fffffffLL || num_segs < 0 || num_segs > T) return SPD_ERR_INVALID_ARG;
+    if (T < 0 || T > kMaxPositions || num_segs < 0 || num_segs > T) return SPD_ERR_INVALID_ARG;
     if ((T > 0) != (num_segs > 0)) return SPD_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(Hq) * T > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(Hq) * T > kMaxPositions) return SPD_ERR_INVALID_ARG;
     return SPD_OK;
 }
 
@@ -209,7 +209,7 @@ int spd_pack_rows(int64_t num_docs, int64_t num_tokens, int micro_bsz, int seq_l
     if ((num_docs == 0) != (num_tokens == 0)) return SPD_ERR_INVALID_ARG;
     const int64_t plen = static_cast<int64_t>(micro_bsz) * seq_len;
     const int64_t r = use_packed_dataset ? (num_tokens + plen - 1) / plen : (num_docs + micro_bsz - 1) / micro_bsz;
-    if (r * plen > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (r * plen > kMaxPositions) return SPD_ERR_INVALID_ARG;
     *rows = r;
     *max_segs = num_docs + 2 * r;
     if (*max_segs > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
@@ -303,7 +303,7 @@ int spd_unpack_data(const int32_t *input_ids, const int32_t *labels, const int32
 {
     if (micro_bsz < 1 || seq_len < 1 || rows < 0) return SPD_ERR_INVALID_ARG;
     const int64_t total = rows * static_cast<int64_t>(micro_bsz) * seq_len;
-    if (total > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (total > kMaxPositions) return SPD_ERR_INVALID_ARG;
     if (rows == 0) return SPD_OK;
     const void *ptrs[] = {input_ids, labels, cu_seqlens, row_seg_ptr, out_ids, out_labels};
     for (const void *p : ptrs)
@@ -330,7 +330,7 @@ int spd_pad_for_sequence_parallel(const int32_t *src, int32_t *dst, int64_t rows
 {
     if (sp_size < 1 || rows < 0 || len < 0 || len > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
     const int64_t padded = (len + sp_size - 1) / sp_size * sp_size;
-    if (rows * padded > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (rows * padded > kMaxPositions) return SPD_ERR_INVALID_ARG;
     if (rows == 0 || padded == 0) return SPD_OK;
     if (!dst || !aligned(dst, 4) || (len > 0 && (!src || !aligned(src, 4)))) return SPD_ERR_INVALID_ARG;
     int sms = 0;
@@ -353,7 +353,7 @@ int spd_split_sequence_parallel(const int32_t *src0, const int32_t *src1, const 
                                 spd_stream_t stream)
 {
     if (sp_size < 1 || rank < 0 || rank >= sp_size || rows < 0 || len < 0) return SPD_ERR_INVALID_ARG;
-    if (len % sp_size != 0 || rows * len > 0x7fffffffLL) return SPD_ERR_INVALID_ARG;
+    if (len % sp_size != 0 || rows * len > kMaxPositions) return SPD_ERR_INVALID_ARG;
     const int32_t *src[3] = {src0, src1, src2};
     int32_t *dst[3] = {dst0, dst1, dst2};
     SplitArgs a = {};
@@ -383,7 +383,7 @@ int spd_rope(uint16_t *q, uint16_t *k, const int32_t *positions, int64_t total_t
              int head_dim, float rope_theta, int inverse, spd_stream_t stream)
 {
     if (head_dim != 64 && head_dim != 128) return SPD_ERR_UNSUPPORTED;
-    if (total_tokens < 0 || total_tokens > 0x7fffffffLL || Hq < 0 || Hkv < 0) return SPD_ERR_INVALID_ARG;
+    if (total_tokens < 0 || total_tokens > kMaxPositions || Hq < 0 || Hkv < 0) return SPD_ERR_INVALID_ARG;
     if ((q && Hq == 0) || (k && Hkv == 0)) return SPD_ERR_INVALID_ARG;
     if (static_cast<int64_t>(Hq > Hkv ? Hq : Hkv) * total_tokens * head_dim > (1LL << 40)) return SPD_ERR_INVALID_ARG;
     if ((q && !aligned(q, 16)) || (k && !aligned(k, 16))) return SPD_ERR_INVALID_ARG;

@@ -39,6 +39,11 @@ inline void prof_end(int which, cudaStream_t s)
 // Workspace header (int32 words): [0] status, [1] work units per head, [2] work
 // counter of the persistent kernels, [3] long units per head (see unit_of).
 constexpr size_t kWsHeader = 256;
+// Largest number of positions (rows x row length) a packing or data-step call
+// accepts: the kernels keep positions in 32 bits and read or write up to one
+// chunk (<= 4096 positions) past the last one before their bounds checks, so
+// the sums must stay below 2^31.
+constexpr long long kMaxPositions = 0x7fffffffLL - 65536;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

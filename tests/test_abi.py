@@ -61,6 +61,22 @@ def test_pack_num_segs_matches_the_oracle(lib):
         ops.pack_num_segs([3, 0, 2], 2, 8, True)
 
 
+def test_position_limit_leaves_a_margin(lib):
+    """Packing and data steps accept at most 2^31 - 65537 positions: the
+    kernels' 32-bit position arithmetic steps up to one chunk past the end."""
+    import ctypes as C
+    from sample_packing_document_gb300 import ops
+    L = ops.load()
+    rows, ms = C.c_int64(0), C.c_int64(0)
+    limit = 2 ** 31 - 65537
+    assert L.spd_pack_rows(1, limit, 1, limit, 1, C.byref(rows), C.byref(ms)) == 0 and rows.value == 1
+    assert L.spd_pack_rows(1, limit + 1, 1, limit + 1, 1, C.byref(rows), C.byref(ms)) == -1
+    fake = C.c_void_p(4096)
+    assert L.spd_pad_for_sequence_parallel(fake, fake, 1, limit + 1, 1, 0, 0, None) == -1
+    assert L.spd_split_sequence_parallel(fake, None, None, 1, limit + 1, 1, 0, fake, None, None, None) == -1
+    assert L.spd_unpack_data(fake, fake, fake, fake, 1, 1, limit + 1, fake, fake, None) == -1
+
+
 def test_pad_for_sequence_parallel_host_checks(lib):
     """Argument checks answered on the host, before any GPU work."""
     import ctypes as C
