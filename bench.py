@@ -10,13 +10,17 @@ the per-document causal mask count: pairs = sum over segments L (L + 1) / 2,
 fwd = 4 d Hq pairs, bwd = 2.5 x fwd (five GEMMs including the S recompute);
 the strict count (bwd = 2 x fwd) is printed beside it.
 
-Default workload: 4 packed rows of 8192 tokens (micro_num 4, micro_bsz 2,
-SEQ_LEN 4096), lognormal document lengths (median 600), 32 q / 32 kv heads,
-head_dim 128, bf16. Inputs (256 MB per tensor) exceed the 129 MB L2, so no
-flush runs between steps.
+Default workload: the load-balance stress case, the largest one that the
+library is measured on: one packed row of 1,048,576 tokens (micro_bsz 1,
+SEQ_LEN 1048576), document lengths 95% uniform [16, 512] and 5% uniform
+[32768, 131072], 4 q / 4 kv heads, head_dim 128, bf16. Inputs (1 GiB per
+tensor) exceed the 129 MB L2, so no flush runs between steps. The three other
+packed workloads (4 x 8192 lognormal, 32K GQA, the 131K sequence-parallel rank
+shape) are timed after it and reported under "per_config".
 
-  python bench.py [--gpus N --steps K --warmup W] [--workload c2|c3|c4|c5|tiny]
+  python bench.py [--gpus N --steps K --warmup W] [--workload c5|c2|c3|c4|tiny]
   python bench.py --impl reference ...     # the CPU oracle as the reference arm
+  python bench.py --cpu-table tiny,c2      # the fp64 oracle over whole workloads (host cores)
 
 Several GPUs (torchrun): each rank runs an independent replica of the same
 step (the path has no exchange step); rank 0 prints the aggregate.
@@ -51,6 +55,7 @@ def peaks():
 # Sources the main backward kernel is compiled from: a recorded DRAM-traffic
 # figure is reported only while their hash matches the one the capture recorded.
 BWD_SOURCES = ("attn_bwd.cu", "ptx.cuh", "internal.h")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "attn_bwd_traffic.json")
 
 
 def kernel_source_hash(files):
@@ -62,29 +67,22 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(summary, files, w):
-    """DRAM bytes per launch of a kernel from its ncu summary under profiles/:
-    the summary states the source hash it was captured at, the bytes per launch
-    and the head count of the captured workload (same documents, fewer heads;
-    traffic grows with the heads, which are independent). None when the file
-    is missing or the kernel's sources changed since."""
+def recorded_traffic(path, files, w):
+    """DRAM bytes per launch of a kernel from a one-pass ncu record (JSON:
+    source hash of the kernel at capture time, the captured workload's
+    documents, q heads, group and head_dim, and dram__bytes_read.sum +
+    dram__bytes_write.sum of one launch). The capture runs the same documents
+    with fewer heads; the heads are independent, so traffic scales with the
+    head count. None when the record is missing, is for other documents or
+    another shape, or the kernel's sources have changed since."""
     try:
-        with open(os.path.join(ROOT, "profiles", summary)) as f:
-            text = f.read()
-    except OSError:
-        return None
-    fields = {}
-    for line in text.splitlines():
-        if line.startswith("traffic-record:"):
-            for kv in line.split(":", 1)[1].split():
-                k, _, v = kv.partition("=")
-                fields[k] = v
-    try:
-        if (fields["source"] != kernel_source_hash(files) or fields["docs"] != w.docs_name
-                or int(fields["group"]) != w.Hq // w.Hkv or int(fields["d"]) != w.head_dim):
+        with open(path) as f:
+            rec = json.load(f)
+        if (rec["source"] != kernel_source_hash(files) or rec["docs"] != w.docs_name
+                or int(rec["group"]) != w.Hq // w.Hkv or int(rec["d"]) != w.head_dim):
             return None
-        return int(fields["dram_bytes"]) * w.Hq // int(fields["hq"])
-    except (KeyError, ValueError):
+        return int(rec["dram_bytes"]) * w.Hq // int(rec["hq"])
+    except (OSError, KeyError, ValueError):
         return None
 
 
@@ -274,9 +272,10 @@ def cpu_baseline(w, seg_lens, target_s=12.0):
     segs, pairs = oracle_sample(w, seg_lens, cu, rate * target_s)
     t = run_oracle_once(q16, k16, v16, do16, cu, segs, scale, cores)
     f = 14.0 * w.head_dim * w.Hq * pairs
-    return {"value": f / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "fp64 oracle fwd+bwd over %d whole segments (%.3g of %.3g unmasked pairs, all %d heads), %.1f s"
-                      % (len(segs), pairs, float(np.sum(seg_lens * (seg_lens + 1.0) / 2)), w.Hq, t),
+    return {"value": f / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": "fp64 oracle fwd+bwd over %d whole segments of the %s documents (%.3g of %.3g unmasked pairs, "
+                      "all %d heads), %.1f s"
+                      % (len(segs), w.name, pairs, float(np.sum(seg_lens * (seg_lens + 1.0) / 2)), w.Hq, t),
             "pack": cpu_pack_baseline()}
 
 
@@ -306,6 +305,51 @@ def cpu_pack_baseline(name="c5", reps=5):
             "sample": "%s documents: %d tokens, %d documents, median of %d calls" % (name, len(toks), len(lens), reps),
             "all_cores": {"GB/s": 2 * cores * nbytes / s_all / 1e9, "cores": cores,
                           "sample": "%d independent packs of the same documents, %d at a time" % (2 * cores, cores)}}
+
+
+def cpu_model():
+    """The host CPU's model name as lscpu prints it (None if unavailable)."""
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    for line in outp.splitlines():
+        if line.strip().lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    return None
+
+
+def cpu_table(names):
+    """The fp64 oracle over whole workloads, forward (every row of every head)
+    and backward (every segment) timed separately on all host cores; one JSON
+    line per workload. Same FLOP convention as the GPU metric (fwd 4 d Hq
+    pairs, bwd 10 d Hq pairs)."""
+    from oracle import attention as OA
+    from oracle import build as OB
+    OB.build()
+    cores = len(os.sched_getaffinity(0))
+    model = cpu_model()
+    for name in names:
+        w, lens, toks = workload_docs(name)
+        seg_lens = segment_lengths(lens, w)
+        fl = flops(seg_lens, w.Hq, w.head_dim)
+        cu = oracle_inputs_for(w, seg_lens)
+        q16, k16, v16, do16 = cpu_inputs(w, int(cu[-1]))
+        t0 = time.perf_counter()
+        packed = OA.pack(toks, lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
+        t_pack = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        OA.attn_fwd(q16, k16, v16, cu, nthreads=cores)
+        t_fwd = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        OA.attn_bwd(q16, k16, v16, do16, cu, nthreads=cores)
+        t_bwd = time.perf_counter() - t0
+        print(json.dumps({"workload": workload_config(w, seg_lens)["workload"], "kind": "oracle", "cores": cores,
+                          "cpu_model": model, "pack_s_one_core": t_pack, "rows": int(packed["rows"]),
+                          "fwd_s": t_fwd, "bwd_s": t_bwd, "fwd_tflops": fl["fwd"] / t_fwd / 1e12,
+                          "fwd_bwd_tflops": fl["total"] / (t_fwd + t_bwd) / 1e12,
+                          "sample": "whole workload, all %d heads" % w.Hq}), flush=True)
+    return 0
 
 
 def run_reference(args):
@@ -366,13 +410,19 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--workload", default="c5")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--only", choices=["pack", "data"], default=None,
                     help="run only the pack (c5 documents) or the data-step measurements and print their JSON "
                          "(for profiling those kernels without the attention step)")
+    ap.add_argument("--cpu-table", default=None,
+                    help="comma-separated workloads: time the fp64 oracle (fwd and bwd) over each whole workload "
+                         "on this host's cores and print one JSON line per workload; no GPU is used")
     args = ap.parse_args()
+    if args.cpu_table:
+        return cpu_table(args.cpu_table.split(","))
     if args.impl == "reference":
         return run_reference(args)
 
@@ -387,7 +437,6 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from sample_packing_document_gb300 import ops
-    from sample_packing_document_gb300 import workloads as W
     if args.only:
         if rank == 0:
             print(json.dumps(pack_measure(ops, dev) if args.only == "pack" else data_measure(ops, dev)))
@@ -396,10 +445,97 @@ def main():
     w, lens, toks = workload_docs(args.workload)
     seg_lens = segment_lengths(lens, w)
     fl = flops(seg_lens, w.Hq, w.head_dim)
+    pk_, how = peaks()
+    burst = pk_.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    sustained = pk_.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+
+    with ClockSampler(local) as clk:
+        r = attn_step_measure(ops, dev, w, lens, toks, args.steps, args.warmup, ws_n, keep_running_s=2.0)
+    clocks = clk.summary(r["host_t0"], r["host_t2"])
+    clocks["window"] = "timed region" + (" + %d identical untimed steps" % r["extra"] if r["extra"] else "")
+    ms = dist_max(r["ms"], ws_n)
+    fwd_ms, bwd_ms = r["fwd_ms"], r["bwd_ms"]
+    value = replica_value(ws_n, fl["total"], ms)
+
+    bwd_tf = fl["bwd"] / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = fl["fwd"] / (fwd_ms * 1e-3) / 1e12
+    roofline = {"kernel": "attn_bwd_kernel (main backward kernel, %d%% of step time)" % round(100 * bwd_ms / ms),
+                "bound": "tensor", "achieved": bwd_tf, "peak": burst, "unit": "TFLOP/s",
+                "frac": bwd_tf / burst, "traffic": recorded_traffic(TRAFFIC_RECORD, BWD_SOURCES, w),
+                "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch from a one-pass ncu "
+                                  "capture of the same documents with one head (profiles/attn_bwd_traffic.json), "
+                                  "scaled by the head count; null once the kernel's sources change",
+                "peak_source": "%s bf16_tflops (burst): the kernel is timed in a loop of a few seconds" % how,
+                "frac_of_sustained": bwd_tf / sustained,
+                "flops_per_launch": fl["bwd"], "ms_per_launch": bwd_ms,
+                "algorithmic": "10 d Hq pairs per launch (pairs = sum over segments L (L + 1) / 2)"}
+
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = {}
+        for name in ("c2", "c3", "c4"):
+            if name == args.workload:
+                continue
+            wc, lc, tc = workload_docs(name)
+            sc = segment_lengths(lc, wc)
+            fc = flops(sc, wc.Hq, wc.head_dim)
+            rc = attn_step_measure(ops, dev, wc, lc, tc, 10, 3, 1)
+            per_config[name] = {
+                "workload": workload_config(wc, sc)["workload"], "value": fc["total"] / (rc["ms"] * 1e-3) / 1e12,
+                "unit": UNIT, "ms_per_step": rc["ms"], "pct_burst": 100 * fc["total"] / (rc["ms"] * 1e-3) / 1e12 / burst,
+                "kernels_ms": {"attn_fwd": rc["fwd_ms"], "attn_bwd": rc["bwd_ms"]},
+                "kernels_tflops": {"attn_fwd": fc["fwd"] / (rc["fwd_ms"] * 1e-3) / 1e12,
+                                   "attn_bwd": fc["bwd"] / (rc["bwd_ms"] * 1e-3) / 1e12},
+                "kernels_pct_burst": {"attn_fwd": 100 * fc["fwd"] / (rc["fwd_ms"] * 1e-3) / 1e12 / burst,
+                                      "attn_bwd": 100 * fc["bwd"] / (rc["bwd_ms"] * 1e-3) / 1e12 / burst},
+                "grad_dtype": "bf16", "steps": 10, "warmup": 3}
+            torch.cuda.empty_cache()
+
+    pack = pack_measure(ops, dev) if rank == 0 else None
+    data_steps = data_measure(ops, dev) if rank == 0 else None
+    torch.cuda.empty_cache()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_measure(args, ops, w, toks, lens, dev, step_ms=ms)
+
+    cpu = None
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, seg_lens)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded documents and N(0,1) q/k/v/dO)",
+                "config": workload_config(w, seg_lens),
+                "pct_bf16_peak": {"burst": 100 * value / ws_n / burst, "sustained": 100 * value / ws_n / sustained},
+                "flops_per_step": fl["total"], "strict_flops_value": ws_n * fl["strict_total"] / (ms * 1e-3) / 1e12,
+                "grad_dtype": "bf16",
+                "kernels_ms": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms},
+                "kernels_tflops": {"attn_fwd": fwd_tf, "attn_bwd": bwd_tf},
+                "kernels_pct_burst": {"attn_fwd": 100 * fwd_tf / burst, "attn_bwd": 100 * bwd_tf / burst},
+                "roofline": roofline, "per_config": per_config, "pack_tokens": pack, "data_steps": data_steps,
+                "clocks": clocks, "e2e": e2e, "gpu_launches": r["launches_per_step"] * args.steps,
+                "cpu_baseline": cpu}
+        print(json.dumps(line))
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def attn_step_measure(ops, dev, w, lens, toks, steps, warmup, ws_n, keep_running_s=0.0):
+    """Times `steps` steps (pack + forward + backward, bf16 gradients) of one
+    workload with inputs resident in HBM: CUDA events on the launching stream
+    around the whole region (barrier + synchronize on both sides) and, recorded
+    by the library, around the forward and backward main kernels of every
+    step. With keep_running_s, the same step keeps running (untimed) until the
+    host window covers that many seconds, so a clock sampler sees it."""
+    import torch
+    from sample_packing_document_gb300 import workloads as W
+    seg_lens = segment_lengths(lens, w)
     T = int(seg_lens.sum())
     d, Hq, Hkv = w.head_dim, w.Hq, w.Hkv
-
-    # inputs resident in HBM
     toks_d = torch.tensor(toks, device=dev)
     lens_d = torch.tensor(lens, device=dev)
     q, k, v, do = W.qkv(T, Hq, Hkv, d, w.seed, device=dev, q_scale=w.q_scale)
@@ -424,7 +560,7 @@ def main():
     # pack: one fused launch (few documents) or scan + stream; fwd: schedule + main;
     # bwd: schedule + pre + main + dq
     launches_per_step = (1 if (w.use_packed_dataset and len(lens) <= 1024) else 2) + 2 + 4
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
     for wsp in (pk["ws"], ws_f, ws_b):
@@ -432,89 +568,47 @@ def main():
         if st != 0:
             raise RuntimeError("device status %d (%s)" % (st, ops.status_string(st)))
 
-    # timed region: K steps, barrier + synchronize on both sides, per-kernel events
     stream = torch.cuda.current_stream()
     ev = {kname: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(args.steps)] for kname in ("fwd", "bwd")}
+                  for _ in range(steps)] for kname in ("fwd", "bwd")}
     for pair in ev["fwd"] + ev["bwd"]:
         for e in pair:
             e.record(stream)    # creates the CUDA event; the library re-records it around its kernel
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    if keep_running_s:
         time.sleep(0.5)                      # nvidia-smi has started sampling
-        dist_barrier(ws_n)
-        torch.cuda.synchronize()
-        host_t0 = time.time()
-        t_start.record(stream)
-        for i in range(args.steps):
-            ops.pack_tokens(toks_d, lens_d, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk)
-            ops.set_profile_events(*ev["fwd"][i], ops.PROFILE_ATTN_FWD)
-            ops.varlen_attn_fwd(q, k, v, cu, ns, out=out, lse=lse, ws=ws_f)
-            ops.set_profile_events(*ev["bwd"][i], ops.PROFILE_ATTN_BWD)
-            ops.varlen_attn_bwd(q, k, v, out, do, lse, cu, ns, dq=dq, dk=dk, dv=dv, ws=ws_b)
-            ops.set_profile_events(None, None, ops.PROFILE_NONE)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        host_t1 = time.time()
-        dist_barrier(ws_n)
-        extra = 0
-        if host_t1 - host_t0 < 2.0:
-            # A short timed region holds few 200 ms samples: keep running the
-            # same step (untimed) so the clock record covers at least 2 s.
-            while time.time() - host_t0 < 2.0:
-                step()
-                torch.cuda.synchronize()
-                extra += 1
-        host_t2 = time.time()
-    clocks = clk.summary(host_t0, host_t2)
-    clocks["window"] = "timed region" + (" + %d identical untimed steps" % extra if extra else "")
-    ms_local = t_start.elapsed_time(t_end) / args.steps
-    ms = dist_max(ms_local, ws_n)
-    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["fwd"])
-    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev["bwd"])
-    value = replica_value(ws_n, fl["total"], ms)
-
-    pk_, how = peaks()
-    peak = pk_.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    bwd_tf = fl["bwd"] / (bwd_ms * 1e-3) / 1e12
-    roofline = {"kernel": "attn_bwd_kernel (main backward kernel, %d%% of step time)" % round(100 * bwd_ms / ms),
-                "bound": "tensor", "achieved": bwd_tf, "peak": peak, "unit": "TFLOP/s",
-                "frac": bwd_tf / peak, "traffic": recorded_traffic("attn_bwd_c2p.md", BWD_SOURCES, w),
-                "traffic_source": "dram__bytes_read.sum + dram__bytes_write.sum per launch, profiles/attn_bwd_c2p.md, "
-                                  "scaled by the head count (null once the kernel's sources change)",
-                "peak_source": "%s bf16_tflops_sustained (kernel timed inside the step loop)" % how,
-                "flops_per_launch": fl["bwd"], "ms_per_launch": bwd_ms}
-    fwd_tf = fl["fwd"] / (fwd_ms * 1e-3) / 1e12
-
-    pack = pack_measure(ops, dev) if rank == 0 else None
-    data_steps = data_measure(ops, dev) if rank == 0 else None
-
-    e2e = None
-    if not args.no_e2e:
-        e2e = e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev)
-
-    cpu = None
-    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, seg_lens)
-
-    if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded documents and N(0,1) q/k/v/dO)",
-                "config": workload_config(w, seg_lens),
-                "pct_bf16_peak": {"sustained": 100 * value / ws_n / peak,
-                                  "burst": 100 * value / ws_n / pk_.get("bf16_tflops", 1900.0)},
-                "flops_per_step": fl["total"], "strict_flops_value": ws_n * fl["strict_total"] / (ms * 1e-3) / 1e12,
-                "kernels_ms": {"attn_fwd": fwd_ms, "attn_bwd": bwd_ms},
-                "kernels_tflops": {"attn_fwd": fwd_tf, "attn_bwd": bwd_tf},
-                "roofline": roofline, "pack_tokens": pack, "data_steps": data_steps, "clocks": clocks, "e2e": e2e,
-                "gpu_launches": launches_per_step * args.steps,
-                "cpu_baseline": cpu}
-        print(json.dumps(line))
-    if ws_n > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
-    return 0
+    dist_barrier(ws_n)
+    torch.cuda.synchronize()
+    host_t0 = time.time()
+    t_start.record(stream)
+    for i in range(steps):
+        ops.pack_tokens(toks_d, lens_d, w.micro_bsz, w.seq_len, w.use_packed_dataset, out=pk)
+        ops.set_profile_events(*ev["fwd"][i], ops.PROFILE_ATTN_FWD)
+        ops.varlen_attn_fwd(q, k, v, cu, ns, out=out, lse=lse, ws=ws_f)
+        ops.set_profile_events(*ev["bwd"][i], ops.PROFILE_ATTN_BWD)
+        ops.varlen_attn_bwd(q, k, v, out, do, lse, cu, ns, dq=dq, dk=dk, dv=dv, ws=ws_b)
+        ops.set_profile_events(None, None, ops.PROFILE_NONE)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    host_t1 = time.time()
+    dist_barrier(ws_n)
+    extra = 0
+    if host_t1 - host_t0 < keep_running_s:
+        # A short timed region holds few 200 ms samples: keep running the
+        # same step (untimed) so the clock record covers the window.
+        while time.time() - host_t0 < keep_running_s:
+            step()
+            torch.cuda.synchronize()
+            extra += 1
+    host_t2 = time.time()
+    for wsp in (pk["ws"], ws_f, ws_b):
+        st = ops.read_status(wsp)
+        if st != 0:
+            raise RuntimeError("device status %d (%s)" % (st, ops.status_string(st)))
+    return {"ms": t_start.elapsed_time(t_end) / steps,
+            "fwd_ms": statistics.mean(a.elapsed_time(b) for a, b in ev["fwd"]),
+            "bwd_ms": statistics.mean(a.elapsed_time(b) for a, b in ev["bwd"]),
+            "host_t0": host_t0, "host_t2": host_t2, "extra": extra, "launches_per_step": launches_per_step}
 
 
 def _time_kernel(ops, which, fn, flush, reps):
@@ -715,7 +809,7 @@ def pack_graph_measure(ops, dev, w, toks_d, lens_d, nbytes, hbm, replays=10):
                       "around the replays" % (nsets, nsets, nsets * nbytes / 1e6, replays)}
 
 
-def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
+def e2e_measure(args, ops, w, toks, lens, dev, step_ms=0.0):
     """Same metric through the public API with host buffers, pipelined the way
     a training loop feeds the GPU: every step copies its documents and q / k /
     v / dO from pinned host memory (copy stream in; dO last, the backward waits
@@ -726,8 +820,11 @@ def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
     the host document lengths (spd_pack_num_segs), so no step waits on the
     device. Timed from before the first copy in to after the last copy out."""
     import torch
+    from sample_packing_document_gb300 import workloads as W
     NB = 3
     ns = ops.pack_num_segs(lens, w.micro_bsz, w.seq_len, w.use_packed_dataset)
+    T = int(np.sum(lens))
+    q, k, v, do = W.qkv(T, w.Hq, w.Hkv, w.head_dim, w.seed, device=dev, q_scale=w.q_scale)
     pin = lambda t: t.cpu().pin_memory()
     toks_h, lens_h = torch.tensor(toks).pin_memory(), torch.tensor(lens).pin_memory()
     in_h = (toks_h, lens_h, pin(q), pin(k), pin(v), pin(do))
@@ -775,10 +872,13 @@ def e2e_measure(args, ops, w, toks, lens, q, k, v, do, dev):
                 dst.copy_(src, non_blocking=True)
             out_read[b].record(s_out)
 
+    del q, k, v, do
     for kk in range(2 * NB):
         step(kk)
     torch.cuda.synchronize()
-    n = max(24, args.steps)    # a window long enough that one fill and one drain weigh little per step
+    # a window long enough that one fill and one drain (the first step's copies
+    # in, the last one's copies out) weigh little per step
+    n = max(24 if step_ms < 50.0 else 8, args.steps)
     a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(s_comp)
     s_in.wait_event(a)                            # no copy of the timed steps starts before `a`

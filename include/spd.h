@@ -122,6 +122,26 @@ int spd_debug_skip_arrive(int which);
  */
 int spd_read_status(const void *ws, spd_stream_t stream, int *device_status);
 
+/*
+ * Inspection hook: synchronise `stream`, then copy to the host the tile
+ * schedule that the last spd_varlen_attn_fwd or spd_varlen_attn_bwd call built
+ * in workspace `ws` (the work list every head's CTAs take units from, longest
+ * first; page "Sample Packing ...", section 5.1: only tiles with unmasked
+ * entries are visited). *num_units (host) receives the number of work units per
+ * head; units (host int32 [capacity][4]; may be NULL if capacity is 0) the first
+ * min(capacity, *num_units) of them, each {segment start, segment end, tile,
+ * cost}, with n = ceil((segment end - segment start) / 128) tiles of 128
+ * tokens in the segment:
+ *   forward:  q tiles `tile` and `tile` + 1 (if < n); q tile i reads kv tiles
+ *             0 .. i; cost = the number of (q tile, kv tile) blocks read;
+ *   backward: kv tile `tile`, which reads q tiles `tile` .. n - 1 of every q
+ *             head of its kv head; cost = n - tile.
+ * Only the diagonal blocks (q tile == kv tile) hold masked entries. Returns
+ * SPD_OK, SPD_ERR_INVALID_ARG or SPD_ERR_CUDA. Not needed for normal use.
+ */
+int spd_attn_read_schedule(const void *ws, spd_stream_t stream, int32_t *num_units, int32_t *units,
+                           int64_t capacity);
+
 /* ------------------------------------------------------------------------- */
 /* Packing                                                                   */
 /* ------------------------------------------------------------------------- */
@@ -369,11 +389,16 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * computes exactly what spd_varlen_attn_fwd computes, with the same argument
  * meaning, layouts and host checks, minus ws / ws_bytes, and allocates nothing.
  * Its scratch (status word and tile work list) is one fixed array of
- * SPD_NOALLOC_SCRATCH_BYTES in the library's device image: every GPU that loads
- * the library holds it until the process exits. Problems whose scratch would
- * not fit (spd_attn_workspace_size(..., bwd = 0) > SPD_NOALLOC_SCRATCH_BYTES;
- * about 250k tiles, e.g. 16M tokens in a few thousand documents) return
- * SPD_ERR_TOO_LARGE before anything is launched.
+ * SPD_NOALLOC_SCRATCH_BYTES (4 MiB) in the library's device image: every GPU
+ * that loads the library holds it until the process exits. The rule is exact:
+ * a problem fits while spd_attn_workspace_size(total_tokens, num_segs, Hq,
+ * Hkv, head_dim, 0) <= SPD_NOALLOC_SCRATCH_BYTES, i.e. 16 bytes per work tile
+ * (ceil(total_tokens / 128) + num_segs tiles) plus 4 bytes per segment and a
+ * 256-byte header stay within 4 MiB: up to about 262,000 tiles, e.g. 33
+ * million tokens in a few thousand documents, but not 16.9 million tokens in
+ * 131,072 documents. A problem that does not fit returns SPD_ERR_TOO_LARGE
+ * before anything is launched; shape and pointer errors are reported first
+ * (SPD_ERR_INVALID_ARG / SPD_ERR_UNSUPPORTED, as for spd_varlen_attn_fwd).
  *
  * The first call on each device looks up the array's device address with that
  * device current (a runtime symbol query, no allocation); make that first call
@@ -384,7 +409,9 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  *
  * device_status (device pointer to one int32, may be NULL) receives the call's
  * device status word (SPD_OK or SPD_ERR_BAD_SEQLENS / SPD_ERR_DEVICE_TIMEOUT),
- * written on `stream` after the kernels.
+ * written on `stream` after the kernels. It is written only when the call
+ * returns SPD_OK: after any other return code it holds whatever it held
+ * before.
  */
 #define SPD_NOALLOC_SCRATCH_BYTES (4u << 20)
 int spd_varlen_attn_fwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,

@@ -200,6 +200,28 @@ int spd_read_status(const void *ws, spd_stream_t stream, int *device_status)
     return SPD_OK;
 }
 
+int spd_attn_read_schedule(const void *ws, spd_stream_t stream, int32_t *num_units, int32_t *units,
+                           int64_t capacity)
+{
+    if (!ws || !num_units || capacity < 0 || (capacity > 0 && !units)) return SPD_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t n = 0;
+    if (cudaMemcpyAsync(&n, static_cast<const int32_t *>(ws) + 1, sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+        return SPD_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SPD_ERR_CUDA;
+    *num_units = n;
+    const int64_t m = n < capacity ? n : capacity;
+    if (m > 0) {
+        static_assert(sizeof(Tile) == 4 * sizeof(int32_t), "Tile is four int32 words");
+        if (cudaMemcpyAsync(units, static_cast<const char *>(ws) + kWsHeader, sizeof(Tile) * static_cast<size_t>(m),
+                            cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return SPD_ERR_CUDA;
+    }
+    return SPD_OK;
+}
+
 int spd_pack_rows(int64_t num_docs, int64_t num_tokens, int micro_bsz, int seq_len, int use_packed_dataset,
                   int64_t *rows, int64_t *max_segs)
 {

@@ -3,7 +3,6 @@
 // to pass). Its scratch -- the status word and the tile work list that
 // spd_varlen_attn_fwd keeps in the caller's workspace -- lives instead in one
 // fixed array of this library's device image.
-#include <atomic>
 #include <mutex>
 
 #include "../../include/spd.h"
@@ -53,6 +52,13 @@ extern "C" int spd_varlen_attn_fwd_noalloc(const uint16_t *q, const uint16_t *k,
         return spd_varlen_attn_fwd(q, k, v, cu_seqlens, num_segs, total_tokens, max_seqlen, Hq, Hkv, head_dim,
                                    softmax_scale, out, lse, nullptr, 0, stream);
     }
+    // Pointer checks of the workspace entry point, made here first so that a
+    // bad pointer reports SPD_ERR_INVALID_ARG whatever the problem size.
+    auto misaligned = [](const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; };
+    if (total_tokens > 0 &&
+        (!q || !k || !v || !out || !lse || !cu_seqlens || misaligned(q, 16) || misaligned(k, 16) ||
+         misaligned(v, 16) || misaligned(out, 16) || misaligned(lse, 4) || misaligned(cu_seqlens, 4)))
+        return SPD_ERR_INVALID_ARG;
     if (need > SPD_NOALLOC_SCRATCH_BYTES) return SPD_ERR_TOO_LARGE;
     void *scratch = nullptr;
     int rc = spd::scratch_on_current_device(&scratch);

@@ -25,6 +25,7 @@ SIGNATURES = {
     "spd_status_string": (ctypes.c_char_p, [_INT]),
     "spd_version": (_INT, []),
     "spd_read_status": (_INT, [_P, _P, ctypes.POINTER(_INT)]),
+    "spd_attn_read_schedule": (_INT, [_P, _P, ctypes.POINTER(_I32), _P, _I64]),
     "spd_set_profile_events": (_INT, [_P, _P, _INT]),
     "spd_debug_skip_arrive": (_INT, [_INT]),
     "spd_pack_rows": (_INT, [_I64, _I64, _INT, _INT, _INT, ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
@@ -103,6 +104,22 @@ def read_status(ws, stream=None):
     v = _INT(0)
     _check("spd_read_status", load().spd_read_status(_ptr(ws), _stream(stream), ctypes.byref(v)))
     return v.value
+
+
+def read_schedule(ws, stream=None):
+    """Synchronise and return the tile schedule of the last attention call on
+    ws as an int32 array [units, 4] of {segment start, segment end, tile, cost}
+    (see spd_attn_read_schedule)."""
+    import numpy as np
+    n = _I32(0)
+    _check("spd_attn_read_schedule", load().spd_attn_read_schedule(_ptr(ws), _stream(stream), ctypes.byref(n),
+                                                                   None, 0))
+    units = np.zeros((max(n.value, 0), 4), np.int32)
+    if n.value > 0:
+        _check("spd_attn_read_schedule",
+               load().spd_attn_read_schedule(_ptr(ws), _stream(stream), ctypes.byref(n),
+                                             units.ctypes.data_as(ctypes.c_void_p), units.shape[0]))
+    return units
 
 
 (PROFILE_NONE, PROFILE_PACK_STREAM, PROFILE_ATTN_FWD, PROFILE_ATTN_BWD, PROFILE_UNPACK, PROFILE_SPLIT,

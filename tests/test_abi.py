@@ -31,6 +31,15 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(ops.SIGNATURES)
 
 
+def test_read_schedule_host_checks(lib):
+    """spd_attn_read_schedule refuses null pointers before touching a GPU."""
+    n = ctypes.c_int32(0)
+    assert lib.spd_attn_read_schedule(None, None, ctypes.byref(n), None, 0) == -1
+    assert lib.spd_attn_read_schedule(ctypes.c_void_p(256), None, None, None, 0) == -1
+    assert lib.spd_attn_read_schedule(ctypes.c_void_p(256), None, ctypes.byref(n), None, 4) == -1
+    assert lib.spd_attn_read_schedule(ctypes.c_void_p(256), None, ctypes.byref(n), None, -1) == -1
+
+
 def test_status_strings_and_version(lib):
     from sample_packing_document_gb300 import ops
     assert lib.spd_version() >= 100

@@ -196,7 +196,7 @@ def test_c_twin_worked_examples():
 @pytest.mark.parametrize("packed", [True, False])
 def test_c_twin_matches_literal_random(packed):
     rng = random.Random(99 + packed)
-    for _ in range(3000):
+    for _ in range(5000):
         mb, sl = rng.randint(1, 4), rng.randint(1, 16)
         docs = _random_docs(rng, 3 * mb * sl, 10)
         f = P.pack_flat(docs, mb, sl, packed)

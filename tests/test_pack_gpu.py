@@ -72,7 +72,7 @@ def test_worked_examples(ops):
 @pytest.mark.parametrize("packed", [True, False])
 def test_random_tiny_cases(ops, packed):
     rng = random.Random(4242 + packed)
-    for _ in range(1500):
+    for _ in range(5000):
         mb, sl = rng.randint(1, 4), rng.randint(1, 16)
         plen = mb * sl
         n = rng.randint(1, 10)

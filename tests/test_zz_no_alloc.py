@@ -67,6 +67,12 @@ def test_noalloc_rejects_oversize_and_reports_bad_seqlens():
                                          P(out.data_ptr()), P(lse.data_ptr()), None,
                                          P(torch.cuda.current_stream().cuda_stream))
     assert rc == -8 and "no-allocation" in ops.status_string(rc)
+    # a null q is a bad argument, reported before the size check
+    rc = lib.spd_varlen_attn_fwd_noalloc(None, P(q.data_ptr()), P(q.data_ptr()), P(q.data_ptr()),
+                                         1 << 17, (1 << 24) + (1 << 17), 0, 2, 2, 128, ctypes.c_float(0.0),
+                                         P(out.data_ptr()), P(lse.data_ptr()), None,
+                                         P(torch.cuda.current_stream().cuda_stream))
+    assert rc == -1
     cu = torch.tensor([0, 200, 100, 256], dtype=torch.int32, device="cuda")
     assert _call_noalloc(lib, q, q, q, cu, 3, out, lse, status) == 0
     torch.cuda.synchronize()
