@@ -125,8 +125,8 @@ int spd_read_status(const void *ws, spd_stream_t stream, int *device_status);
 /*
  * Inspection hook: synchronise `stream`, then copy to the host the tile
  * schedule that the last spd_varlen_attn_fwd or spd_varlen_attn_bwd call built
- * in workspace `ws` (the work list every head's CTAs take units from, longest
- * first; page "Sample Packing ...", section 5.1: only tiles with unmasked
+ * in workspace `ws` (the work list every head's CTAs take units from, sorted by
+ * cost, largest first; page "Sample Packing ...", section 5.1: only tiles with unmasked
  * entries are visited). *num_units (host) receives the number of work units per
  * head; units (host int32 [capacity][4]; may be NULL if capacity is 0) the first
  * min(capacity, *num_units) of them, each {segment start, segment end, tile,
@@ -134,8 +134,11 @@ int spd_read_status(const void *ws, spd_stream_t stream, int *device_status);
  * tokens in the segment:
  *   forward:  q tiles `tile` and `tile` + 1 (if < n); q tile i reads kv tiles
  *             0 .. i; cost = the number of (q tile, kv tile) blocks read;
- *   backward: kv tile `tile`, which reads q tiles `tile` .. n - 1 of every q
- *             head of its kv head; cost = n - tile.
+ *   backward: if bit 30 of `tile` is set, the one kv tile t = `tile` with
+ *             that bit cleared, cost = n - t; else the pair of kv tiles `tile`
+ *             and n - 1 - `tile`, cost = n + 1 (a segment's pairs sit in
+ *             consecutive entries, in order). Kv tile t reads q tiles t .. n - 1
+ *             of every q head of its kv head.
  * Only the diagonal blocks (q tile == kv tile) hold masked entries. Returns
  * SPD_OK, SPD_ERR_INVALID_ARG or SPD_ERR_CUDA. Not needed for normal use.
  */

@@ -114,7 +114,12 @@ int check_attn_shape(int64_t T, int32_t num_segs, int Hq, int Hkv, int D)
     return SPD_OK;
 }
 
-size_t bwd_delta_off(int64_t T, int32_t num_segs) { return align_up(schedule_ws_bytes(T, num_segs), 256); }
+// backward workspace: schedule, the scheduler's segment order, D, dQ accumulator
+size_t bwd_order_off(int64_t T, int32_t num_segs) { return align_up(schedule_ws_bytes(T, num_segs), 256); }
+size_t bwd_delta_off(int64_t T, int32_t num_segs)
+{
+    return bwd_order_off(T, num_segs) + align_up(sizeof(int32_t) * static_cast<size_t>(num_segs + 1), 256);
+}
 size_t bwd_acc_off(int64_t T, int32_t num_segs, int Hq)
 {
     return bwd_delta_off(T, num_segs) + align_up(sizeof(float) * static_cast<size_t>(Hq) * T, 256);
@@ -490,7 +495,7 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     if (rc != SPD_OK) return rc;
     if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
 
-    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, 2, sms, ws, s));
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, 2, sms, Hkv, ws, nullptr, s));
     if (rc != SPD_OK) return rc;
     AttnFwdArgs a = {};
     if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
@@ -538,7 +543,10 @@ int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     if (rc != SPD_OK) return rc;
     if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
 
-    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 1, 1, sms, ws, s));
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 1, 1, sms, Hkv, ws,
+                                 reinterpret_cast<int32_t *>(static_cast<char *>(ws) +
+                                                             bwd_order_off(total_tokens, num_segs)),
+                                 s));
     if (rc != SPD_OK) return rc;
     AttnBwdArgs a = {};
     if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;

@@ -12,9 +12,10 @@
 //   bwd_pre_kernel   D_i = rowsum(dO * O) (fp32) and zeroes the fp32 dQ
 //                    accumulator, laid out [Hq][d / 32][T][32]; runs beside the
 //                    tile schedule (programmatic dependent launch).
-//   attn_bwd_kernel  one CTA per (128-row kv tile, kv head): K, V stay in shared
-//                    memory; the CTA walks every (q head of the group, q tile
-//                    from the diagonal to the segment end). Per step, five
+//   attn_bwd_kernel  persistent; a work unit is a (kv head, 128-row kv tile):
+//                    K, V stay in shared memory while the CTA walks every (q
+//                    head of the group, q tile from the diagonal to the segment
+//                    end, upward or downward). Per step, five
 //                    tcgen05 MMAs with fp32 accumulation in TMEM:
 //                      S^T = K Q^T           region A (P^T is then written over it, bf16)
 //                      dP^T = V dO^T         region B
@@ -180,6 +181,21 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float *__restrict__ d
     }
 }
 
+// A work unit in flight: {kv head (-1: no more work), segment start, segment
+// end, kv tile | kDescBit}. Kv tile t reads q tiles t .. n - 1 of its segment,
+// in ascending order, or in descending order (n - 1 down to t) when kDescBit
+// is set: the second kv tile of a scheduled pair walks down, so that the CTAs
+// working through one document's pairs touch nearby q tiles at any moment.
+constexpr int kDescBit = 1 << 30;
+__device__ __forceinline__ int seg_tiles(const int4 &u) { return (u.z - u.y + kTile - 1) / kTile; }
+__device__ __forceinline__ int unit_kv_tile(const int4 &u) { return u.w & (kDescBit - 1); }
+__device__ __forceinline__ int unit_nq(const int4 &u) { return seg_tiles(u) - unit_kv_tile(u); }
+// q tile (inside the segment) of the unit's j-th q-tile step, 0 <= j < unit_nq
+__device__ __forceinline__ int unit_q_tile(const int4 &u, int j)
+{
+    return (u.w & kDescBit) ? seg_tiles(u) - 1 - j : unit_kv_tile(u) + j;
+}
+
 // dV (P warps, IS_P) or dK (dS warps) rows of a finished unit's kv tile: the
 // calling warp's 32 rows (TMEM lanes 32 quarter ..), d columns [half * D/2,
 // half * D/2 + D/2), read from TMEM at `acc`. With bf16 grads and d = 128, a
@@ -193,7 +209,7 @@ __device__ __forceinline__ void store_acc_rows(const AttnBwdArgs &a, uint32_t ac
                                             const uint8_t *slot)
 {
     const int lane = threadIdx.x & 31;
-    const int row0 = u.y + u.w * kTile + quarter * 32;
+    const int row0 = u.y + unit_kv_tile(u) * kTile + quarter * 32;
     const int kj = row0 + lane;
     const float mul = IS_P ? 1.f : a.scale;
     if (D == 128 && a.store_tma && row0 + 32 <= u.z) {
@@ -251,7 +267,6 @@ __device__ __forceinline__ void store_acc_rows(const AttnBwdArgs &a, uint32_t ac
 }
 
 // ------------------------------------------------------------------ main kernel
-__device__ __forceinline__ int seg_tiles(const int4 &u) { return (u.z - u.y + kTile - 1) / kTile; }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_constant__ AttnBwdArgs a)
@@ -331,13 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
     setmaxnreg_dec<kControlRegs>();
     if (warp == 16) {
         // ------------------------------------------------------------ producer
-        // Takes work units (kv head, kv tile) from the shared counter in list
-        // order (unit_of): the few units much longer than a kv head's share of an
-        // SM first, across kv heads; then kv-head-major, so the CTAs of one kv
-        // head run together and the Q / dO tiles they share and the dQ rows they
-        // add into stay in L2; longest first inside a head. Q / dO stream through a 2-stage ring that
-        // runs on across units; the next unit's K / V are pulled into L2 as soon
-        // as it is taken and copied in once the last MMA reading K has completed.
+        // Takes work units (kv head, pair of kv tiles) from the shared counter in
+        // list order (unit_of): the few units much longer than a kv head's share
+        // of an SM first, across kv heads; then kv-head-major, so the CTAs of one
+        // kv head run together and the Q / dO tiles they share and the dQ rows
+        // they add into stay in L2; longest segment first inside a head, a
+        // segment's pairs in order. Every pair of a segment costs the same, so the
+        // CTAs on one document stay in step, the first tiles walking up and the
+        // second ones down through nearby q tiles. Q / dO stream through a
+        // 2-stage ring that runs on across units; the next unit's K / V are
+        // pulled into L2 as soon as it is taken and copied in once the last MMA
+        // reading K has completed.
         if (lane == 0) {
             const int n_tiles = *a.tile_count;
             const int total_units = n_tiles * a.Hkv;
@@ -348,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
             auto load_step = [&](const int4 &d, int nq, int i, int gs) -> bool {
                 const int st = gs % kQStages, u = gs / kQStages;
                 const int h = d.x * group + i / nq;
-                const int q0 = d.y + (d.w + i % nq) * kTile;
+                const int q0 = d.y + unit_q_tile(d, i % nq) * kTile;
                 if (u > 0 && !mbar_wait(&sm.q_empty[st], (u - 1) & 1, abort_flag, a.status)) return false;
                 mbar_arrive_expect_tx(&sm.q_full[st], kTileBytes);
                 for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q[st][c], &a.tm_q, c * 64, h, q0, &sm.q_full[st]);
@@ -361,26 +380,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 return true;
             };
             bool ok = true;
+            int4 pending = make_int4(-1, 0, 0, 0);   // second kv tile of the pair taken last
             for (int it = 0; ok; ++it) {
                 const int slot = it & 1;
                 if (it >= 2 && !mbar_wait(&sm.unit_empty[slot], ((it >> 1) - 1) & 1, abort_flag, a.status)) break;
-                const int w = *abort_flag ? total_units : atomicAdd(a.work_counter, 1);
                 int4 d = make_int4(-1, 0, 0, 0);
-                if (w < total_units) {
-                    int head, idx;
-                    unit_of(w, n_tiles, n_long, a.Hkv, head, idx);
-                    const Tile tl = a.tiles[idx];
-                    d = make_int4(head, tl.seg_start, tl.seg_end, tl.t);
+                if (pending.x >= 0 && !*abort_flag) {
+                    d = pending;
+                    pending.x = -1;
+                } else {
+                    // A scheduled unit is one kv tile, or the pair of kv tiles p and
+                    // n - 1 - p of one segment: n + 1 q-tile steps together, the same
+                    // for every pair of the segment.
+                    const int w = *abort_flag ? total_units : atomicAdd(a.work_counter, 1);
+                    if (w < total_units) {
+                        int head, idx;
+                        unit_of(w, n_tiles, n_long, a.Hkv, head, idx);
+                        const Tile tl = a.tiles[idx];
+                        const int n = (tl.seg_end - tl.seg_start + kTile - 1) / kTile;
+                        d = make_int4(head, tl.seg_start, tl.seg_end, tl.t & ~kSingleTile);
+                        if (!(tl.t & kSingleTile))
+                            pending = make_int4(head, tl.seg_start, tl.seg_end, (n - 1 - tl.t) | kDescBit);
+                    }
                 }
                 sm.unit[slot] = d;
                 mbar_arrive(&sm.unit_full[slot]);
                 if (d.x < 0) break;
-                const int k0 = d.y + d.w * kTile;
+                const int k0 = d.y + unit_kv_tile(d) * kTile;
                 for (int c = 0; c < D / 64; ++c) {
                     tma_prefetch_l2_3d(&a.tm_k, c * 64, d.x, k0);
                     tma_prefetch_l2_3d(&a.tm_v, c * 64, d.x, k0);
                 }
-                const int nq = seg_tiles(d) - d.w;
+                const int nq = unit_nq(d);
                 const int nsteps = group * nq;
                 if (!load_step(d, nq, 0, gi)) break;
                 if (it > 0 && !mbar_wait(&sm.kv_empty, (it - 1) & 1, abort_flag, a.status)) break;
@@ -454,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 const int4 d = sm.unit[slot];
                 mbar_arrive(&sm.unit_empty[slot]);
                 if (d.x < 0) break;
-                const int nsteps = group * (seg_tiles(d) - d.w);
+                const int nsteps = group * unit_nq(d);
                 ok = mbar_wait(&sm.kv_full, it & 1, abort_flag, a.status) && issue_s(gi) && issue_dp(gi);
                 for (int i = 0; ok && i < nsteps; ++i, ++gi) {
                     const int st = gi % kQStages;
@@ -524,9 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         const uint32_t ds_addr = smem_u32(sm.ds[0]);
         const bool loader = half == 0;                            // loads the step's LSE / D column t
         auto col_term = [&](const int4 &u, int i) -> float {
-            const int nq = seg_tiles(u) - u.w;
+            const int nq = unit_nq(u);
             const int h = u.x * group + i / nq;
-            const int qi = u.y + (u.w + i % nq) * kTile + t;
+            const int qi = u.y + unit_q_tile(u, i % nq) * kTile + t;
             if (qi >= a.total_tokens) return 0.f;
             const size_t x = static_cast<size_t>(h) * a.total_tokens + qi;
             return is_p ? -a.lse[x] * 1.4426950408889634f : a.delta[x];   // P warps keep -LSE log2 e
@@ -562,12 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
         float nxt = (ok && loader && cur.x >= 0) ? col_term(cur, 0) : 0.f;
         int gi = 0;
         for (int it = 0; ok && cur.x >= 0; ++it) {
-            const int nq = seg_tiles(cur) - cur.w;
+            const int nq = unit_nq(cur);
             const int nsteps = group * nq;
-            const int kj = cur.y + cur.w * kTile + t;
+            const int kj = cur.y + unit_kv_tile(cur) * kTile + t;
             for (int i = 0; i < nsteps; ++i, ++gi) {
                 const int h = cur.x * group + i / nq;
-                const int q0 = cur.y + (cur.w + i % nq) * kTile;
+                const int q0 = cur.y + unit_q_tile(cur, i % nq) * kTile;
                 const uint32_t ph = gi & 1;
                 float *colbuf = is_p ? sm.lse2[gi & 1] : sm.delta[gi & 1];
                 uint64_t *colbar = is_p ? &sm.cols_l[gi & 1] : &sm.cols_d[gi & 1];

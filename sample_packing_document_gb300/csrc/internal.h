@@ -133,9 +133,9 @@ struct LossArgs {
 cudaError_t launch_loss(const LossArgs &a, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tile schedule
-// One work tile: a 128-token block of one segment. Sorted by cost, largest
-// first. `cost` is the number of 128-blocks of the segment a tile touches in
-// the forward direction (tile t of a segment: t + 1).
+// One work unit of the tile schedule: tiles of one segment (see
+// launch_schedule for the forward and backward meaning of `t`); `cost` is the
+// number of (q tile, kv tile) blocks the unit computes.
 struct Tile {
     int32_t seg_start;
     int32_t seg_end;
@@ -144,6 +144,7 @@ struct Tile {
 };
 
 constexpr int kTile = 128;
+constexpr int kSingleTile = 1 << 30;   // backward schedule: Tile.t names one kv tile, not a pair
 
 // Upper bound of the tile count for total_tokens tokens in num_segs segments.
 inline int64_t max_tiles(int64_t total_tokens, int64_t num_segs)
@@ -153,9 +154,13 @@ inline int64_t max_tiles(int64_t total_tokens, int64_t num_segs)
 
 // Builds the work list into the workspace (after the header): validates
 // cu_seqlens (status SPD_ERR_BAD_SEQLENS on failure) and writes the unit count
-// to ws[1]. order: 0 = forward costs, 1 = backward costs (n - t). unit: tiles
-// per work unit (2 = a pair of consecutive q tiles, forward only); Tile.t is
-// the unit's first tile.
+// to ws[1]. Units are sorted by cost, largest first. order 0 (forward): unit =
+// tiles per work unit (2 = a pair of consecutive q tiles), Tile.t the unit's
+// first q tile. order 1 (backward): Tile.t with kSingleTile set is the single
+// kv tile t & ~kSingleTile (cost n - t); otherwise the pair of kv tiles Tile.t
+// and n - 1 - Tile.t of a segment of n tiles (cost n + 1), the pairs of a
+// segment in consecutive slots; heads = kv heads of the launch; seg_order
+// (num_segs + 1 int32 of scratch) is required.
 // Work unit w of `heads` x n_tiles, the tile list of every head sorted by cost
 // (largest first): the first n_long tiles of every head (the units much longer
 // than a head's share of one SM) come first, interleaved across heads so the
@@ -175,7 +180,8 @@ __device__ __forceinline__ void unit_of(int w, int n_tiles, int n_long, int head
 }
 
 cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
-                            int order, int unit, int num_sms, void *ws, cudaStream_t stream);
+                            int order, int unit, int num_sms, int heads, void *ws, int32_t *seg_order,
+                            cudaStream_t stream);
 size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs);
 
 // ---------------------------------------------------------------- attention

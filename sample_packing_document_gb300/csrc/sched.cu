@@ -4,16 +4,25 @@
 // attention per document (page "Sample Packing: attention problems of
 // long-sequence LLM training", section 5.1 "FlashAttention"), so a tile never
 // spans two segments and only the tiles of each document's own causal
-// triangle are ever visited. In the forward pass, q tile t of a segment reads
-// kv tiles 0..t (cost t + 1); in the backward pass, kv tile t reads q tiles
-// t..n-1 of its segment (cost n - t). Listing tiles by decreasing cost
-// (longest-processing-time first) lets the many short tiles fill in behind
-// the few long ones when documents are very uneven.
+// triangle are ever visited. Listing work by decreasing cost
+// (longest-processing-time first) lets the many short units fill in behind the
+// few long ones when documents are very uneven.
 //
-// One CTA: validates cu_seqlens, counts work units per segment (exclusive scan
-// -> unit offsets), then a counting sort by cost over all units in parallel. A
-// unit is one tile (backward, and forward with unit = 1) or two consecutive q
-// tiles of a segment that one forward CTA computes together (unit = 2).
+// Forward (order 0): a unit is two consecutive q tiles t, t + 1 of a segment
+// that one CTA computes together; q tile i reads kv tiles 0 .. i, so the cost is
+// (t + 1) + (t + 2). Units are counting-sorted by cost over all units.
+//
+// Backward (order 1): kv tile t reads q tiles t .. n - 1 (cost n - t). In a
+// long segment that is still short against one SM's share of the launch, the
+// kv tiles p and n - 1 - p form one unit (cost n + 1, the same for every pair of the
+// segment): the CTAs that take a document's pairs together also finish
+// together and walk nearby q tiles meanwhile (the first tile of a pair upward
+// from its diagonal, the second downward to its diagonal), so the Q / dO tiles
+// and dQ rows they share stay in L2. Longer segments keep one unit per kv tile,
+// so that the longest-first list can still balance them.
+//
+// One CTA: validates cu_seqlens, counts work per segment, sorts, writes the
+// list; the sort and the list are built in parallel by all threads.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -22,6 +31,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kCostCap = 4 * kThreads - 1;  // costs above this share one bin (order among them is free)
+constexpr int kPairMin = 16;                // backward: segments of at least this many tiles may be paired
 
 __device__ long long block_scan_excl(long long v, long long *total, long long *sh)
 {
@@ -53,7 +63,7 @@ __device__ long long block_scan_excl(long long v, long long *total, long long *s
 __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, int32_t nsegs,
                                                             int64_t T, int order, int unit, int num_sms,
                                                             int *status, int32_t *count, Tile *tiles,
-                                                            int32_t *tile_off)
+                                                            int32_t *tile_off, int32_t *seg_order, int heads)
 {
     // The backward's preprocessing kernel depends on nothing computed here: let
     // it start at once (programmatic dependent launch; it waits for this grid
@@ -100,6 +110,98 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
         }
         return;
     }
+    if (order) {
+        // ---------------------------------------------------- backward
+        // A segment of n kv tiles is "paired" when it is long (n >= kPairMin:
+        // its q tiles and dQ rows do not all stay in L2 while its kv tiles are
+        // worked through) but its pair cost n + 1 is at most a quarter of one
+        // SM's share of the whole launch: its kv tiles p and n - 1 - p form one
+        // unit (the middle tile of an odd n stays single), and its pairs take
+        // consecutive slots of their cost bin, in order. Other segments keep one
+        // unit per kv tile (cost n - t): short ones gain nothing from pairing,
+        // and very long ones need the finer grain for the longest-first list to
+        // balance them. Units are counting-sorted by cost over everything.
+        unsigned long long my_cost = 0;
+        for (int sg = tid; sg < nsegs; sg += kThreads) {
+            const long long n = (cu[sg + 1] - cu[sg] + kTile - 1) / kTile;
+            my_cost += static_cast<unsigned long long>(n * (n + 1) / 2);
+        }
+        atomicAdd(&total_cost, my_cost);
+        __syncthreads();
+        const long long c_pair =
+            max(2LL, static_cast<long long>(total_cost) * heads / (4LL * num_sms));
+        auto paired = [&](long long n) { return n >= kPairMin && n + 1 <= c_pair; };
+        // counts: one per single tile, floor(n / 2) per paired segment in bin n + 1
+        for (int sg = tid; sg < nsegs; sg += kThreads) {
+            const long long n = (cu[sg + 1] - cu[sg] + kTile - 1) / kTile;
+            if (paired(n)) atomicAdd(&bins[static_cast<int>(min(n + 1, static_cast<long long>(kCostCap)))],
+                                     static_cast<int>(n / 2));
+        }
+        for (int i = tid; i < static_cast<int>(carry); i += kThreads) {
+            int lo = 0, hi = nsegs;  // largest segment with tile_off[s] <= i
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (tile_off[mid] <= i) lo = mid;
+                else hi = mid;
+            }
+            const int n = (cu[lo + 1] - cu[lo] + kTile - 1) / kTile, t = i - tile_off[lo];
+            if (!paired(n) || (n & 1 && 2 * t + 1 == n)) atomicAdd(&bins[min(n - t, kCostCap)], 1);
+        }
+        __syncthreads();
+        {
+            const long long c_long = max(4LL, (2LL * static_cast<long long>(total_cost) + num_sms - 1) / num_sms);
+            int n_long = 0;
+            if (c_long <= kCostCap)
+                for (int c = static_cast<int>(c_long) + tid; c <= kCostCap; c += kThreads) n_long += bins[c];
+            if (n_long) atomicAdd(&count[2], n_long);
+            int v[4], sum = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[k] = bins[kCostCap - (4 * tid + k)];
+                sum += v[k];
+            }
+            long long tot;
+            long long run = block_scan_excl(sum, &tot, sh);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                bins[kCostCap - (4 * tid + k)] = static_cast<int>(run);
+                run += v[k];
+            }
+            if (tid == 0) *count = static_cast<int32_t>(tot);
+        }
+        __syncthreads();
+        // slots: a paired segment reserves floor(n / 2) consecutive ones
+        for (int sg = tid; sg < nsegs; sg += kThreads) {
+            const long long n = (cu[sg + 1] - cu[sg] + kTile - 1) / kTile;
+            if (paired(n))
+                seg_order[sg] = atomicAdd(&bins[static_cast<int>(min(n + 1, static_cast<long long>(kCostCap)))],
+                                          static_cast<int>(n / 2));
+        }
+        __syncthreads();
+        for (int i = tid; i < static_cast<int>(carry); i += kThreads) {
+            int lo = 0, hi = nsegs;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (tile_off[mid] <= i) lo = mid;
+                else hi = mid;
+            }
+            const int n = (cu[lo + 1] - cu[lo] + kTile - 1) / kTile, t = i - tile_off[lo];
+            Tile w;
+            w.seg_start = cu[lo];
+            w.seg_end = cu[lo + 1];
+            if (paired(n) && 2 * t + 1 < n) {          // first tile of pair t
+                w.t = t;
+                w.cost = n + 1;
+                tiles[seg_order[lo] + t] = w;
+            } else if (!paired(n) || 2 * t + 1 == n) {  // a single tile
+                w.t = t | kSingleTile;
+                w.cost = n - t;
+                tiles[atomicAdd(&bins[min(n - t, kCostCap)], 1)] = w;
+            }
+        }
+        return;
+    }
+
     const int ntiles = static_cast<int>(carry);
 
     auto locate = [&](int i, int &s, int &t, int &n, int &cost) {
@@ -112,8 +214,7 @@ __global__ void __launch_bounds__(kThreads) schedule_kernel(const int32_t *cu, i
         s = lo;
         t = (i - tile_off[s]) * unit;                       // first tile of the unit
         n = (cu[s + 1] - cu[s] + kTile - 1) / kTile;        // tiles of the segment
-        if (order) cost = n - t;                            // backward: q tiles t .. n-1
-        else cost = (t + 1) + (unit > 1 && t + 1 < n ? t + 2 : 0);  // forward: kv tiles of each q tile
+        cost = (t + 1) + (unit > 1 && t + 1 < n ? t + 2 : 0);  // kv tiles of each q tile
     };
 
     unsigned long long my_cost = 0;
@@ -176,8 +277,10 @@ size_t schedule_ws_bytes(int64_t total_tokens, int32_t num_segs)
 }
 
 cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
-                            int order, int unit, int num_sms, void *ws, cudaStream_t stream)
+                            int order, int unit, int num_sms, int heads, void *ws, int32_t *seg_order,
+                            cudaStream_t stream)
 {
+    if (order && !seg_order) return cudaErrorInvalidValue;
     char *base = reinterpret_cast<char *>(ws);
     int *status = reinterpret_cast<int *>(base);
     int32_t *count = reinterpret_cast<int32_t *>(base) + 1;
@@ -185,7 +288,8 @@ cudaError_t launch_schedule(const int32_t *cu_seqlens, int32_t num_segs, int64_t
     int32_t *tile_off = reinterpret_cast<int32_t *>(
         base + kWsHeader + align_up(sizeof(Tile) * static_cast<size_t>(max_tiles(total_tokens, num_segs)), 256));
     schedule_kernel<<<1, kThreads, 0, stream>>>(cu_seqlens, num_segs, total_tokens, order, unit,
-                                                num_sms > 0 ? num_sms : 1, status, count, tiles, tile_off);
+                                                num_sms > 0 ? num_sms : 1, status, count, tiles, tile_off,
+                                                seg_order, heads > 0 ? heads : 1);
     return cudaGetLastError();
 }
 

@@ -298,6 +298,9 @@ def test_long_document_whole_compare(ops):
     _check_full(ops, [33000, 700, 5, 1], 2, 1, 128, seed=13, grad_dtype=torch.bfloat16)
 
 
+SINGLE = 1 << 30     # backward schedule: the unit is one kv tile, not a pair
+
+
 def _blocks_of_schedule(units, bwd):
     """(segment start, q tile, kv tile) blocks the schedule visits, from the
     unit meaning spd_attn_read_schedule documents."""
@@ -305,7 +308,8 @@ def _blocks_of_schedule(units, bwd):
     for a, b, t, cost in units.tolist():
         n = -(-(b - a) // 128)
         if bwd:
-            got = [(a, i, t) for i in range(t, n)]
+            kvs = [t & ~SINGLE] if t & SINGLE else sorted({t, n - 1 - t})
+            got = [(a, i, kv) for kv in kvs for i in range(kv, n)]
         else:
             got = [(a, i, j) for i in (t, t + 1) if i < n for j in range(i + 1)]
         assert cost == len(got), (a, b, t, cost)
@@ -327,6 +331,7 @@ def _unmasked_pairs(a, b, qi, kj):
     ([3, 4, 5, 4], 4, 41),               # the page's documents 3, 4, 5, 4: 41 kept entries of 136
     ([16384, 16384], 16512, None),       # two 16K documents in 32K: 16512 tiles of 65536 (74.80% skipped)
     ([300, 1, 129, 517, 2, 128, 1000], None, None),
+    ([20000, 2048, 2100, 4000, 77, 3000], None, None),   # long and short: the backward pairs kv tiles
 ])
 def test_schedule_visits_exactly_the_unmasked_tiles(ops, lens, blocks_per_head, pairs):
     """The work lists the forward and backward kernels run, read back from the
@@ -348,6 +353,14 @@ def test_schedule_visits_exactly_the_unmasked_tiles(ops, lens, blocks_per_head, 
     for ws, bwd in ((ws_f, False), (ws_b, True)):
         units = ops.read_schedule(ws)
         assert np.all(np.diff(units[:, 3]) <= 0)              # longest first
+        if bwd:                                                # a segment's pairs in consecutive slots, in order
+            pair = (units[:, 2] & SINGLE) == 0
+            if lens[0] == 20000:
+                assert pair.sum() > 0
+            for a in np.unique(units[pair, 0]):
+                ts = units[pair & (units[:, 0] == a), 2]
+                assert ts.tolist() == list(range(len(ts)))
+                assert np.all(np.diff(np.flatnonzero(pair & (units[:, 0] == a))) == 1)
         blocks = _blocks_of_schedule(units, bwd)
         assert len(blocks) == len(set(blocks))                 # each block once
         assert set(blocks) == want                             # exactly the blocks with unmasked entries
