@@ -689,6 +689,26 @@ def data_measure(ops, dev, reps=20):
     out["rope"] = {"workload": "c2 q / k in place: %d tokens, %d + %d heads, d %d, positions = indexes" % (
         T, w.Hq, w.Hkv, w.head_dim), "ms": ms, "bytes": int(nbytes), "GB/s": nbytes / (ms * 1e-3) / 1e9,
         "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    # RoPE fused into the forward attention's prologue, against the same forward without RoPE and
+    # against the unfused path (the RoPE pass over q and k, then the forward): c2's batch, 32 / 32 heads
+    v = torch.randn((T, w.Hkv, w.head_dim), device=dev).to(torch.bfloat16)
+    ns = int(packed["num_segs"].item())
+    cu_t = packed["cu_seqlens"][:ns + 1].contiguous()
+    ws_f = ops.workspace(ops.attn_workspace_size(T, ns, w.Hq, w.Hkv, w.head_dim, False), dev)
+    o_buf = torch.empty_like(q)
+    l_buf = torch.empty(w.Hq, T, dtype=torch.float32, device=dev)
+    ms_plain = _time_kernel(ops, ops.PROFILE_ATTN_FWD, lambda: ops.varlen_attn_fwd(q, k, v, cu_t, ns, out=o_buf,
+                                                                                   lse=l_buf, ws=ws_f), flush, reps)
+    ms_fused = _time_kernel(ops, ops.PROFILE_ATTN_FWD, lambda: ops.varlen_attn_fwd_rope(
+        q, k, v, cu_t, ns, rope_theta=10000.0, out=o_buf, lse=l_buf, ws=ws_f), flush, reps)
+    out["rope_fused_forward"] = {
+        "workload": "c2 batch (%d tokens, %d / %d heads, d %d), positions restarting at every segment" % (
+            T, w.Hq, w.Hkv, w.head_dim),
+        "forward_ms": ms_plain, "forward_with_rope_ms": ms_fused,
+        "unfused_rope_pass_ms": out["rope"]["ms"],
+        "saved_ms": ms_plain + out["rope"]["ms"] - ms_fused,
+        "timing": "main forward kernel (CUDA events recorded by the library), L2 flushed, median of %d" % reps}
+    del v, o_buf, l_buf
     # masked token loss and its gradient over the c2 batch's labels (the same pack), synthetic bf16 logits
     # over a 50000-token vocabulary (the token ids' range)
     V = 50000

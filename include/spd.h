@@ -365,6 +365,30 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         spd_stream_t stream);
 
 /*
+ * spd_varlen_attn_fwd with rotary position embedding fused into its prologue:
+ * the attention of RoPE(q), RoPE(k) and v, where every q and k row is rotated
+ * by its position inside its segment, p = i - cu_seqlens[s] for token i of
+ * segment s (positions restart at every document, page "Sample Packing ...",
+ * section 4.1, reset_position_id; for the cu_seqlens of spd_pack_tokens these
+ * positions are exactly its `indexes`). The rotation is the one spd_rope applies
+ * (rotate-half: channel j < head_dim/2 with channel j + head_dim/2, angle
+ * p * rope_theta^(-2j/head_dim); rope_theta <= 0 means 10000), done on each Q and
+ * K tile in shared memory after its copy lands and before the tensor cores read
+ * it; the rotated tiles are rounded to bf16 like spd_rope's output, and never
+ * written to HBM (the XTuner page "序列并行", Figure 1 pseudo code, applies
+ * apply_rotary_pos_emb to q and k right before the attention call). q and k are
+ * read, not modified. Arguments, layouts, workspace and errors as for
+ * spd_varlen_attn_fwd. The backward of this forward is spd_varlen_attn_bwd on
+ * spd_rope-rotated copies of q and k (same positions, e.g. the pack's indexes),
+ * followed by spd_rope(..., inverse = 1) on dq and dk.
+ */
+int spd_varlen_attn_fwd_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                             const int32_t *cu_seqlens, int32_t num_segs, int64_t total_tokens,
+                             int32_t max_seqlen, int Hq, int Hkv, int head_dim, float softmax_scale,
+                             float rope_theta, uint16_t *out, float *lse, void *ws, size_t ws_bytes,
+                             spd_stream_t stream);
+
+/*
  * Backward of spd_varlen_attn_fwd: with P_ij = exp(S_ij - lse_i),
  * D_i = dout_i . out_i and dS_ij = P_ij (dout_i . v_j - D_i):
  *   dq_i = scale sum_j dS_ij k_j,

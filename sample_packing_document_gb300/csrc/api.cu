@@ -157,6 +157,61 @@ int take_debug_skip(int which)
 
 using namespace spd;
 
+// The forward call with or without the in-kernel RoPE rotation of q and k.
+static int attn_fwd_impl(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                         int32_t num_segs, int64_t total_tokens, int Hq, int Hkv, int head_dim,
+                         float softmax_scale, int rope, float rope_theta, uint16_t *out, float *lse, void *ws,
+                         size_t ws_bytes, spd_stream_t stream)
+{
+    int rc = check_attn_shape(total_tokens, num_segs, Hq, Hkv, head_dim);
+    if (rc != SPD_OK) return rc;
+    if (!ws || !aligned(ws, 256)) return SPD_ERR_WORKSPACE;
+    if (ws_bytes < spd_attn_workspace_size(total_tokens, num_segs, Hq, Hkv, head_dim, 0)) return SPD_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (total_tokens == 0) return clear_status(ws, s);
+    if (!q || !k || !v || !out || !lse || !cu_seqlens) return SPD_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+        !aligned(cu_seqlens, 4))
+        return SPD_ERR_INVALID_ARG;
+    int sms = 0;
+    rc = require_sm103(&sms);
+    if (rc != SPD_OK) return rc;
+    if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
+
+    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, 2, sms, Hkv, ws, nullptr, s));
+    if (rc != SPD_OK) return rc;
+    AttnFwdArgs a = {};
+    if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_k, k, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_o, out, total_tokens, Hq, head_dim, 32)) != SPD_OK) return rc;
+    if ((rc = make_map(&a.tm_v, v, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
+    char *base = static_cast<char *>(ws);
+    a.out = out;
+    a.lse = lse;
+    a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
+    a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
+    a.work_counter = reinterpret_cast<int32_t *>(base) + 2;
+    a.long_count = reinterpret_cast<const int32_t *>(base) + 3;
+    a.status = reinterpret_cast<int *>(base);
+    a.total_tokens = static_cast<int32_t>(total_tokens);
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.scale = softmax_scale;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.debug_skip = take_debug_skip(SPD_DEBUG_SKIP_FWD_Q);
+    a.rope = rope;
+    if (rope) {
+        const double base = rope_theta > 0.f ? static_cast<double>(rope_theta) : 10000.0;
+        for (int j = 0; j < head_dim / 2; ++j) {
+            // turns per position, theta_j / (2 pi) < 1/6, as 64-bit fixed point
+            const double turns = std::pow(base, -2.0 * j / head_dim) / (2.0 * 3.141592653589793238462643);
+            a.freq[j] = static_cast<unsigned long long>(std::ldexp(turns, 64));
+        }
+    }
+    return cuda_rc(launch_attn_fwd(a, head_dim, (total_tokens + 2 * kTile - 1) / (2 * kTile) + num_segs, s));
+}
+
+
 extern "C" {
 
 const char *spd_status_string(int s)
@@ -480,43 +535,18 @@ int spd_varlen_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         spd_stream_t stream)
 {
     (void)max_seqlen;
-    int rc = check_attn_shape(total_tokens, num_segs, Hq, Hkv, head_dim);
-    if (rc != SPD_OK) return rc;
-    if (!ws || !aligned(ws, 256)) return SPD_ERR_WORKSPACE;
-    if (ws_bytes < spd_attn_workspace_size(total_tokens, num_segs, Hq, Hkv, head_dim, 0)) return SPD_ERR_WORKSPACE;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (total_tokens == 0) return clear_status(ws, s);
-    if (!q || !k || !v || !out || !lse || !cu_seqlens) return SPD_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
-        !aligned(cu_seqlens, 4))
-        return SPD_ERR_INVALID_ARG;
-    int sms = 0;
-    rc = require_sm103(&sms);
-    if (rc != SPD_OK) return rc;
-    if (!(softmax_scale > 0.f)) softmax_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
+    return attn_fwd_impl(q, k, v, cu_seqlens, num_segs, total_tokens, Hq, Hkv, head_dim, softmax_scale, 0, 0.f,
+                         out, lse, ws, ws_bytes, stream);
+}
 
-    rc = cuda_rc(launch_schedule(cu_seqlens, num_segs, total_tokens, 0, 2, sms, Hkv, ws, nullptr, s));
-    if (rc != SPD_OK) return rc;
-    AttnFwdArgs a = {};
-    if ((rc = make_map(&a.tm_q, q, total_tokens, Hq, head_dim)) != SPD_OK) return rc;
-    if ((rc = make_map(&a.tm_k, k, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
-    if ((rc = make_map(&a.tm_o, out, total_tokens, Hq, head_dim, 32)) != SPD_OK) return rc;
-    if ((rc = make_map(&a.tm_v, v, total_tokens, Hkv, head_dim)) != SPD_OK) return rc;
-    char *base = static_cast<char *>(ws);
-    a.out = out;
-    a.lse = lse;
-    a.tiles = reinterpret_cast<const Tile *>(base + kWsHeader);
-    a.tile_count = reinterpret_cast<const int32_t *>(base) + 1;
-    a.work_counter = reinterpret_cast<int32_t *>(base) + 2;
-    a.long_count = reinterpret_cast<const int32_t *>(base) + 3;
-    a.status = reinterpret_cast<int *>(base);
-    a.total_tokens = static_cast<int32_t>(total_tokens);
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.scale = softmax_scale;
-    a.scale_log2 = softmax_scale * 1.4426950408889634f;
-    a.debug_skip = take_debug_skip(SPD_DEBUG_SKIP_FWD_Q);
-    return cuda_rc(launch_attn_fwd(a, head_dim, (total_tokens + 2 * kTile - 1) / (2 * kTile) + num_segs, s));
+int spd_varlen_attn_fwd_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v, const int32_t *cu_seqlens,
+                             int32_t num_segs, int64_t total_tokens, int32_t max_seqlen, int Hq, int Hkv,
+                             int head_dim, float softmax_scale, float rope_theta, uint16_t *out, float *lse,
+                             void *ws, size_t ws_bytes, spd_stream_t stream)
+{
+    (void)max_seqlen;
+    return attn_fwd_impl(q, k, v, cu_seqlens, num_segs, total_tokens, Hq, Hkv, head_dim, softmax_scale, 1,
+                         rope_theta, out, lse, ws, ws_bytes, stream);
 }
 
 int spd_varlen_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *out,

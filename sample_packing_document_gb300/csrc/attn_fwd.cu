@@ -24,6 +24,11 @@
 //                    memory), O_X += P_X(j) V_j (P from TMEM, V from shared
 //                    memory), interleaved A / B so one tile's softmax overlaps
 //                    the other tile's MMAs.
+//   warps 10-11      with RoPE only: rotate Q_A, Q_B and every K tile in shared
+//                    memory once its copy has landed and before any MMA reads
+//                    it (rotate-half form, channel j with j + d/2, angle p *
+//                    theta_j, p = the row's position inside its segment), so the
+//                    rotated q and k never go through HBM. Without RoPE they idle.
 // TMEM: S_A / P_A [0,128), S_B / P_B [128,256), O_A [256, 256+d), O_B [384, 384+d).
 // Each tile's MMAs run in issue order on the tensor pipe, so S_X(j+1), issued
 // after O_X += P_X(j) V_j, never overwrites P_X(j) before it has been read, and
@@ -44,6 +49,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kSoftmaxRegs = 216, kControlRegs = 72;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;  // bytes of one [128 rows][64 bf16] swizzled atom
+constexpr int kRotWarps = 2;           // warps 10-11: RoPE rotation of the Q / K tiles in shared memory
 
 template <int D>
 struct alignas(1024) FwdSmem {
@@ -51,8 +57,8 @@ struct alignas(1024) FwdSmem {
     uint8_t k[kStages][D / 64][kAtom];
     uint8_t v[kStages][D / 64][kAtom];
     uint8_t ostage[8][32 * 128];   // per softmax warp: 32 rows x 64 d of O (bf16, 128-byte swizzle)
-    uint64_t q_full, q_empty;
-    uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+    uint64_t q_full, q_empty, q_rot;
+    uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages], k_rot[kStages];
     uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
     uint64_t unit_full[2], unit_empty[2];
     int4 unit[2];               // work unit in flight: {head (-1: no more work), seg_start, seg_end, first tile}
@@ -106,11 +112,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
         mbar_init(&sm.q_empty, 1);
+        mbar_init(&sm.q_rot, kRotWarps);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.k_full[s], 1);
             mbar_init(&sm.v_full[s], 1);
             mbar_init(&sm.k_empty[s], 1);
             mbar_init(&sm.v_empty[s], 1);
+            mbar_init(&sm.k_rot[s], kRotWarps);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.s_full[x], 1);
@@ -118,7 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(&sm.o_done[x], 1);
             mbar_init(&sm.o_free[x], 4);
             mbar_init(&sm.unit_full[x], 1);
-            mbar_init(&sm.unit_empty[x], 9);   // MMA thread + one lane of each softmax warp
+            // MMA thread + one lane of each softmax warp (+ each rotator warp with RoPE)
+            mbar_init(&sm.unit_empty[x], a.rope ? 9 + kRotWarps : 9);
         }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
@@ -265,8 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         umma_bf16_ts_step(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, vd, kk * (2048 >> 4), idesc_o,
                                           (j > 0 || kk > 0) ? 1u : 0u);
                 };
-                ok = mbar_wait(&sm.q_full, it & 1, abort_flag, a.status) &&
-                     mbar_wait(&sm.k_full[kv_iter % kStages], (kv_iter / kStages) & 1, abort_flag, a.status);
+                // with RoPE, the operands are ready once rotated in place
+                uint64_t *const q_ready = a.rope ? &sm.q_rot : &sm.q_full;
+                uint64_t *const k_ready = a.rope ? sm.k_rot : sm.k_full;
+                ok = mbar_wait(q_ready, it & 1, abort_flag, a.status) &&
+                     mbar_wait(&k_ready[kv_iter % kStages], (kv_iter / kStages) & 1, abort_flag, a.status);
                 if (!ok) break;
                 tc_fence_after();
                 issue_s(0, 0);                        // S regions: the last P V of each tile ran before
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     const int st = kvj % kStages;
                     const bool next_k = j + 1 < us.n_kv;
                     if (!mbar_wait(&sm.v_full[st], (kvj / kStages) & 1, abort_flag, a.status)) { ok = false; break; }
-                    if (next_k && !mbar_wait(&sm.k_full[(kvj + 1) % kStages], ((kvj + 1) / kStages) & 1, abort_flag,
+                    if (next_k && !mbar_wait(&k_ready[(kvj + 1) % kStages], ((kvj + 1) / kStages) & 1, abort_flag,
                                              a.status)) {
                         ok = false;
                         break;
@@ -325,6 +337,82 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (v_commits[s] > 0) wait_drain(&sm.v_empty[s], (v_commits[s] - 1) & 1);
             }
             if (q_commits > 0) wait_drain(&sm.q_empty, (q_commits - 1) & 1);
+        }
+    } else if (a.rope) {
+        // ------------------------------------------------------------ RoPE rotators
+        // 64 threads rotate a [128 rows][D] tile in place: thread tau takes the
+        // 16-byte chunk c of the first half of every row r0 + kStride * k (8
+        // channel pairs j = 8c .. 8c + 7, each with its partner j + D/2 at the same
+        // swizzled offset of the second 64-column atom for D = 128, or chunk c + 4
+        // of the same atom for D = 64). The angle of row r is (p0 + r) theta_j for
+        // a tile starting p0 tokens into its segment: exact for the thread's first
+        // row (64-bit fixed-point phase, as spd_rope computes it), then stepped
+        // from row to row by the fixed rotation kStride theta_j.
+        constexpr int kCh = D / 16, kStride = 64 / kCh, kRows = 128 / kStride;
+        const int tau = threadIdx.x - 320;
+        const int c = tau % kCh, r0 = tau / kCh;
+        auto exact_cs = [&](uint32_t p, int e, float &cs, float &sn) {
+            const uint64_t ph = static_cast<uint64_t>(p) * a.freq[c * 8 + e];   // turns * 2^64, mod 2^64
+            const int32_t half_turns = static_cast<int32_t>(static_cast<uint32_t>(ph >> 32));
+            sincospif(static_cast<float>(half_turns) * 4.656612873077393e-10f, &sn, &cs);
+        };
+        float stc[8], sts[8];   // rotation by kStride positions
+#pragma unroll
+        for (int e = 0; e < 8; ++e) exact_cs(kStride, e, stc[e], sts[e]);
+        auto rotate_tile = [&](uint8_t (*tile)[kAtom], int p0) {
+            float zc[8], zs[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) exact_cs(static_cast<uint32_t>(p0 + r0), e, zc[e], zs[e]);
+            const uint32_t lo_base = smem_u32(tile[0]);
+            const uint32_t hi_base = D == 128 ? smem_u32(tile[D / 128]) : lo_base;
+#pragma unroll 2
+            for (int k = 0; k < kRows; ++k) {
+                const int row = r0 + kStride * k;
+                const uint32_t lo_addr = lo_base + row * 128 + ((c ^ (row & 7)) << 4);
+                const uint32_t hi_addr = hi_base + row * 128 + (((D == 128 ? c : c + 4) ^ (row & 7)) << 4);
+                uint32_t lo[4], hi[4], olo[4], ohi[4];
+                ld_shared_v4(lo_addr, lo[0], lo[1], lo[2], lo[3]);
+                ld_shared_v4(hi_addr, hi[0], hi[1], hi[2], hi[3]);
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const int e0 = 2 * w, e1 = 2 * w + 1;
+                    const float x0 = __uint_as_float(lo[w] << 16), x1 = __uint_as_float(lo[w] & 0xffff0000u);
+                    const float y0 = __uint_as_float(hi[w] << 16), y1 = __uint_as_float(hi[w] & 0xffff0000u);
+                    olo[w] = pack_bf16x2(x0 * zc[e0] - y0 * zs[e0], x1 * zc[e1] - y1 * zs[e1]);
+                    ohi[w] = pack_bf16x2(y0 * zc[e0] + x0 * zs[e0], y1 * zc[e1] + x1 * zs[e1]);
+                }
+                st_shared_v4(lo_addr, olo[0], olo[1], olo[2], olo[3]);
+                st_shared_v4(hi_addr, ohi[0], ohi[1], ohi[2], ohi[3]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {   // advance every angle by kStride positions
+                    const float nc = zc[e] * stc[e] - zs[e] * sts[e];
+                    zs[e] = zs[e] * stc[e] + zc[e] * sts[e];
+                    zc[e] = nc;
+                }
+            }
+            fence_proxy_async_smem();   // the tensor core reads these operands next
+            __syncwarp();
+        };
+        uint32_t kv_iter = 0;
+        for (int it = 0;; ++it) {
+            const int slot = it & 1;
+            if (!warp_wait(&sm.unit_full[slot], (it >> 1) & 1, abort_flag, a.status)) break;
+            const int4 d = sm.unit[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.unit_empty[slot]);
+            if (d.x < 0) break;
+            const UnitShape us = unit_shape(d);
+            if (!warp_wait(&sm.q_full, it & 1, abort_flag, a.status)) break;
+            for (int x = 0; x < (us.has_b ? 2 : 1); ++x) rotate_tile(sm.q[x], (us.tA + x) * kTile);
+            if (lane == 0) mbar_arrive(&sm.q_rot);
+            bool ok = true;
+            for (int j = 0; j < us.n_kv; ++j, ++kv_iter) {
+                const int st = kv_iter % kStages;
+                if (!warp_wait(&sm.k_full[st], (kv_iter / kStages) & 1, abort_flag, a.status)) { ok = false; break; }
+                rotate_tile(sm.k[st], j * kTile);
+                if (lane == 0) mbar_arrive(&sm.k_rot[st]);
+            }
+            if (!ok) break;
         }
     }
     } else {

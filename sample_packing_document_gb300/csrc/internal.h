@@ -201,6 +201,8 @@ struct AttnFwdArgs {
     float scale_log2;    // softmax_scale * log2(e)
     float scale;
     int debug_skip;      // test hook: the producer leaves its first Q load out
+    int rope;            // 1: rotate Q and K in shared memory by their in-segment positions (RoPE)
+    unsigned long long freq[64];  // RoPE turns per position of pair j as 64-bit fixed point (j < d/2)
 };
 
 cudaError_t launch_attn_fwd(const AttnFwdArgs &a, int head_dim, int64_t grid_tiles,

@@ -36,6 +36,8 @@ SIGNATURES = {
     "spd_varlen_attn_fwd": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _P, _P, _P, _SZ, _P]),
     "spd_varlen_attn_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _INT,
                                    _P, _P, _P, _P, _SZ, _P]),
+    "spd_varlen_attn_fwd_rope": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _F32, _P, _P, _P,
+                                        _SZ, _P]),
     "spd_varlen_attn_fwd_noalloc": (_INT, [_P, _P, _P, _P, _I32, _I64, _I32, _INT, _INT, _INT, _F32, _P, _P, _P,
                                            _P]),
     "spd_unpack_data": (_INT, [_P, _P, _P, _P, _I64, _INT, _INT, _P, _P, _P]),
@@ -328,6 +330,27 @@ def varlen_attn_fwd(q, k, v, cu_seqlens, num_segs, max_seqlen=0, softmax_scale=N
     _check("spd_varlen_attn_fwd", load().spd_varlen_attn_fwd(
         _ptr(_as_u16(q)), _ptr(_as_u16(k)), _ptr(_as_u16(v)), _ptr(cu_seqlens), int(num_segs), T, int(max_seqlen),
         Hq, Hkv, d, scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+    return out, lse
+
+
+def varlen_attn_fwd_rope(q, k, v, cu_seqlens, num_segs, rope_theta=10000.0, max_seqlen=0, softmax_scale=None,
+                         out=None, lse=None, ws=None, stream=None):
+    """spd_varlen_attn_fwd_rope: the forward pass on RoPE-rotated q and k, the
+    rotation (per-document positions from cu_seqlens) done inside the kernel.
+    Returns (out bf16 [T, Hq, d], lse fp32 [Hq, T])."""
+    _need_cuda(q, k, v, cu_seqlens)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, T, dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(attn_workspace_size(T, num_segs, Hq, Hkv, d, False), q.device)
+    scale = 0.0 if softmax_scale is None else float(softmax_scale)
+    _check("spd_varlen_attn_fwd_rope", load().spd_varlen_attn_fwd_rope(
+        _ptr(_as_u16(q)), _ptr(_as_u16(k)), _ptr(_as_u16(v)), _ptr(cu_seqlens), int(num_segs), T, int(max_seqlen),
+        Hq, Hkv, d, scale, float(rope_theta), _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
     return out, lse
 
 
