@@ -824,9 +824,52 @@ def pack_graph_measure(ops, dev, w, toks_d, lens_d, nbytes, hbm, replays=10):
         raise RuntimeError("pack status")
     ms = a.elapsed_time(b) / (replays * nsets)
     gbs = nbytes / (ms * 1e-3) / 1e9
+    del sets
+    copy = same_traffic_copy(dev, toks_d.numel(), nbytes, hbm, replays)
     return {"ms_per_pack": ms, "GB/s": gbs, "frac_hbm": gbs / hbm, "frac_8TBs": gbs / 8000.0,
             "timing": "one CUDA graph of %d packs over %d buffer sets (%.0f MB, > 2x L2), %d replays, CUDA events "
-                      "around the replays" % (nsets, nsets, nsets * nbytes / 1e6, replays)}
+                      "around the replays" % (nsets, nsets, nsets * nbytes / 1e6, replays),
+            "same_traffic_copy": copy, "frac_of_copy": copy["ms_per_call"] / ms}
+
+
+def same_traffic_copy(dev, n, nbytes, hbm, replays=10):
+    """What a plain copy of the pack's traffic shape reaches at the same size in
+    the same harness: torch's copy kernel reading n int32 and writing them three
+    times (4 B read + 12 B written per position, one launch per call), in a CUDA
+    graph over rotating buffer sets larger than twice the L2. The HBM copy peak
+    is measured on 1 GiB; at a few MB per launch, launch and ramp latency bound
+    any kernel below it, and this is that bound."""
+    import torch
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
+    per = 16 * n
+    nsets = max(4, int(2 * l2 // per) + 2)
+    sets = [(torch.randint(0, 50000, (n,), dtype=torch.int32, device=dev),
+             torch.empty((3, n), dtype=torch.int32, device=dev)) for _ in range(nsets)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def run():
+        for src, dst in sets:
+            dst.copy_(src.unsqueeze(0).expand(3, n))
+
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (replays * nsets)
+    return {"ms_per_call": ms, "GB/s": per / (ms * 1e-3) / 1e9, "frac_hbm": per / (ms * 1e-3) / 1e9 / hbm,
+            "bytes": per, "what": "torch copy_ of int32 [n] into [3, n], n = %d, %d sets in one graph" % (n, nsets)}
 
 
 def e2e_measure(args, ops, w, toks, lens, dev, step_ms=0.0):

@@ -472,8 +472,15 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
     }
 }
 
-__global__ void __launch_bounds__(kFusedThreads) pack_fused_kernel(PackArgs a)
+// At most 32 registers per thread (8 resident CTAs per SM): the 1025 CTAs of a
+// million-token row then run as one wave. Launched as a programmatic dependent
+// of whatever precedes it on the stream: it lets the next launch be scheduled
+// at once and waits for the previous grid (and its memory) before its first
+// global access, so back-to-back packs overlap launch latency only.
+__global__ void __launch_bounds__(kFusedThreads, 8) pack_fused_kernel(PackArgs a)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ int32_t s_start[kFusedDocs + 1];
     __shared__ int sh[32];
     __shared__ int bad_s;
@@ -651,11 +658,19 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
 
     const long long npos = static_cast<long long>(a.rows) * a.plen;
     if (a.packed && a.num_docs >= 1 && a.num_docs <= kFusedDocs && a.rows <= kFusedRows) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(1 + (npos + kFusedChunk - 1) / kFusedChunk));
+        cfg.blockDim = dim3(kFusedThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         prof_begin(kProfPackStream, stream);
-        pack_fused_kernel<<<static_cast<unsigned>(1 + (npos + kFusedChunk - 1) / kFusedChunk), kFusedThreads, 0,
-                            stream>>>(a);
+        cudaError_t e0 = cudaLaunchKernelEx(&cfg, pack_fused_kernel, a);
         prof_end(kProfPackStream, stream);
-        return cudaGetLastError();
+        return e0;
     }
     pack_scan_kernel<<<1, kScanThreads, 0, stream>>>(a, aux);
     cudaError_t e = cudaGetLastError();
