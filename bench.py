@@ -470,6 +470,13 @@ def main():
                 "flops_per_launch": fl["bwd"], "ms_per_launch": bwd_ms,
                 "algorithmic": "10 d Hq pairs per launch (pairs = sum over segments L (L + 1) / 2)"}
 
+    # end to end through the public API with host buffers, right after the
+    # device-resident measurement of the same workload
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_measure(args, ops, w, toks, lens, dev, step_ms=ms)
+        torch.cuda.empty_cache()
+
     per_config = None
     if rank == 0 and not args.no_per_config:
         per_config = {}
@@ -494,10 +501,6 @@ def main():
     pack = pack_measure(ops, dev) if rank == 0 else None
     data_steps = data_measure(ops, dev) if rank == 0 else None
     torch.cuda.empty_cache()
-
-    e2e = None
-    if not args.no_e2e:
-        e2e = e2e_measure(args, ops, w, toks, lens, dev, step_ms=ms)
 
     cpu = None
     if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
@@ -943,21 +946,26 @@ def e2e_measure(args, ops, w, toks, lens, dev, step_ms=0.0):
     # in, the last one's copies out) weigh little per step
     n = max(24 if step_ms < 50.0 else 8, args.steps)
     a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(s_comp)
-    s_in.wait_event(a)                            # no copy of the timed steps starts before `a`
-    for kk in range(n):
-        step(kk)
-    for bb in range(NB):
-        s_comp.wait_event(out_read[bb])           # every read-back has landed
-    bev.record(s_comp)
-    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.5)                           # nvidia-smi has started sampling
+        host_t0 = time.time()
+        a.record(s_comp)
+        s_in.wait_event(a)                        # no copy of the timed steps starts before `a`
+        for kk in range(n):
+            step(kk)
+        for bb in range(NB):
+            s_comp.wait_event(out_read[bb])       # every read-back has landed
+        bev.record(s_comp)
+        torch.cuda.synchronize()
+        host_t1 = time.time()
+    clocks = clk.summary(host_t0, host_t1)
     if ops.read_status(ws_b) != 0 or ops.read_status(pk["ws"]) != 0:
         raise RuntimeError("e2e status")
     ms = a.elapsed_time(bev) / n
     h2d = sum(x.numel() * x.element_size() for x in in_h)
     d2h = sum(x.numel() * x.element_size() for x in out_h[0])
     return {"value": fl["total"] / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "clocks": clocks,
             "pipeline": "%d buffer sets; copies in / compute / copies out on three streams (dO after the "
                         "forward's inputs); segment count from the host document lengths; %d steps timed from the "
                         "first copy in to the last copy out" % (NB, n)}
