@@ -70,6 +70,9 @@ struct PackArgs {
     int32_t *doc_out;   // first output position of each document (+ sentinel)
     int32_t *doc_in;    // first input position of each document
     int32_t *doc_keep;  // tokens kept of each document
+    int32_t *aligned;   // build_pack: documents d' in [1, d) that start on a row start (+ total at [num_docs])
+    unsigned *ticket;            // build_pack prefix kernel: CTA order counter
+    unsigned long long *look;    // build_pack prefix kernel: 2 x CTAs look-back descriptors
     int vec_out;        // 1: output pointers are 16-byte aligned
     int vec_in;         // 1: tokens is 16-byte aligned
 };

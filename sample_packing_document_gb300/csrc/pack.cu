@@ -10,16 +10,24 @@
 //
 // build_pack with at most 1024 documents and 512 rows runs as one fused
 // launch (pack_fused_kernel). Otherwise, two launches on one stream:
-//   pack_scan_kernel    one CTA: prefix sums over the document lengths, the
-//                       document -> output position map, cu_seqlens,
-//                       row_seg_ptr, max_seqlen, num_segs. Work ~ num_docs.
-//   pack_packed_stream_kernel (build_pack) / unpack_stream_kernel (build_unpack)
-//                       all SMs: the token stream, 16-byte vector stores of
-//                       input_ids / labels / indexes. Work ~ output positions.
-// The stream kernel is a programmatic dependent launch: in build_pack mode it
-// loads its tokens and stores input_ids (which needs no document boundaries)
-// while the scan runs, then waits for the scan's results before labels and
-// indexes.
+//   build_pack:
+//     pack_prefix_kernel  prefix sums of the document lengths (document starts)
+//                         and of the "starts on a row start" flags, 4096
+//                         documents per CTA, CTAs chained by a decoupled
+//                         look-back; num_segs, the last row's end; zeroes
+//                         max_seqlen. Work ~ num_docs.
+//     pack_packed_stream_kernel  all SMs: the token stream (input_ids, labels,
+//                         indexes in 16-byte stores) and the segment fields of
+//                         the boundaries inside each CTA's chunk (cu_seqlens,
+//                         row_seg_ptr, max_seqlen). Work ~ output positions.
+//   build_unpack:
+//     pack_scan_kernel    one CTA: prefix sums, the document -> output position
+//                         map and every segment field.
+//     unpack_stream_kernel  all SMs: the token stream.
+// The stream kernels are programmatic dependent launches: in build_pack mode
+// the stream kernel loads its tokens and stores input_ids (which needs no
+// document boundaries) while the prefix kernel runs, then waits for its
+// results before labels, indexes and the segment fields.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -28,7 +36,6 @@ namespace {
 
 constexpr int kScanThreads = 1024;
 constexpr int kScanItems = 4;  // documents per thread per pass
-constexpr int kScanSmemDocs = 8192;   // build_pack: document offsets staged in shared memory up to this count
 constexpr int kStreamThreads = 256;
 constexpr int kStreamIters = 4;
 constexpr int kChunk = kStreamThreads * 4 * kStreamIters;  // positions per CTA
@@ -60,6 +67,146 @@ __device__ long long block_excl_scan(long long v, long long *total, long long *s
     *total = sh[31];
     __syncthreads();  // sh is reused by the next call
     return warp_excl + x - v;
+}
+
+// ---------------------------------------------------------------- build_pack prefix
+constexpr int kPrefixDocs = kScanThreads * kScanItems;   // documents per prefix CTA
+
+// Decoupled look-back over the prefix CTAs (thread 0 of each): publish this
+// CTA's aggregate, add up the predecessors' published values back to the
+// first inclusive one, publish the inclusive prefix. A CTA only waits on CTAs
+// that took their order ticket earlier, which are running, so the chain ends;
+// the wait is bounded all the same (status SPD_ERR_DEVICE_TIMEOUT). Values are
+// clamped below 2^40 (valid inputs stay below 2^31).
+__device__ long long lookback_excl(unsigned long long *look, int bid, long long agg, int *status)
+{
+    constexpr unsigned long long kAgg = 1ull << 62, kInc = 2ull << 62, kVal = (1ull << 62) - 1;
+    const unsigned long long v = static_cast<unsigned long long>(agg < (1LL << 40) ? agg : (1LL << 40));
+    if (bid == 0) {
+        st_release_u64(look, kInc | v);
+        return 0;
+    }
+    st_release_u64(look + bid, kAgg | v);
+    long long excl = 0;
+    int j = bid - 1;
+    const uint64_t t0 = globaltimer_ns();
+    while (j >= 0) {
+        const unsigned long long w = ld_acquire_u64(look + j);
+        const unsigned long long state = w >> 62;
+        if (state == 2) {
+            excl += static_cast<long long>(w & kVal);
+            break;
+        }
+        if (state == 1) {
+            excl += static_cast<long long>(w & kVal);
+            --j;
+            continue;
+        }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_status(status, kErrTimeout);
+            break;
+        }
+    }
+    const long long inc = excl + static_cast<long long>(v);
+    st_release_u64(look + bid, kInc | static_cast<unsigned long long>(inc < (1LL << 40) ? inc : (1LL << 40)));
+    return excl;
+}
+
+__global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, int nb)
+{
+    // The stream kernel may load its tokens and store input_ids meanwhile.
+    pdl_launch_dependents();
+    __shared__ long long sh[33];
+    __shared__ long long s_excl[2];   // this CTA's exclusive prefix: document starts, aligned starts
+    __shared__ int s_bid, bad_s;
+    const int tid = threadIdx.x;
+    const int nd = a.num_docs, rows = a.rows;
+    const long long plen = a.plen, total = a.num_tokens;
+    if (tid == 0) {
+        if (nb == 1) *a.status = 0;   // several CTAs: the host cleared it
+        s_bid = nb > 1 ? static_cast<int>(atomicAdd(a.ticket, 1u)) : 0;
+        bad_s = 0;
+    }
+    __syncthreads();
+    const int bid = s_bid;
+    for (long long r = static_cast<long long>(bid) * kScanThreads + tid; r < rows;
+         r += static_cast<long long>(nb) * kScanThreads)
+        a.max_seqlen[r] = 0;
+
+    // document starts
+    const int d0 = bid * kPrefixDocs + tid * kScanItems;
+    int len[kScanItems];
+    long long sum = 0;
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        const int d = d0 + k;
+        len[k] = d < nd ? a.doc_lens[d] : 0;
+        if (d < nd && len[k] <= 0) bad = true;
+        if (len[k] < 0) len[k] = 0;
+        sum += len[k];
+    }
+    long long agg;
+    const long long e = block_excl_scan(sum, &agg, sh);
+    if (tid == 0) s_excl[0] = lookback_excl(a.look, bid, agg, a.status);
+    __syncthreads();
+    long long start[kScanItems];
+    long long run = s_excl[0] + e;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        start[k] = run;
+        run += len[k];
+    }
+    // documents (other than the first) that start on a row start: the same
+    // boundary as the row start, counted so the boundary ranks stay exact
+    int flag[kScanItems], fsum = 0;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        const int d = d0 + k;
+        flag[k] = (d >= 1 && d < nd && start[k] % plen == 0) ? 1 : 0;
+        fsum += flag[k];
+    }
+    long long fagg;
+    const long long fe = block_excl_scan(fsum, &fagg, sh);
+    if (tid == 0) s_excl[1] = lookback_excl(a.look + nb, bid, fagg, a.status);
+    __syncthreads();
+    long long frun = s_excl[1] + fe;
+#pragma unroll
+    for (int k = 0; k < kScanItems; ++k) {
+        const int d = d0 + k;
+        if (d < nd) {
+            a.doc_out[d] = static_cast<int32_t>(start[k]);
+            a.doc_in[d] = static_cast<int32_t>(start[k]);
+            a.aligned[d] = static_cast<int32_t>(frun);
+        }
+        frun += flag[k];
+    }
+    if (bad) atomicOr(&bad_s, 1);
+    __syncthreads();
+    if (tid == 0) {
+        bool fail = bad_s != 0;
+        if (bid == nb - 1) {
+            // The CTA holding the last document knows the totals: the end of the
+            // last document, the segment count (rows, plus one per document start
+            // not on a row start, plus the padding tail), the last row's end.
+            const long long tot_len = s_excl[0] + agg, tot_al = s_excl[1] + fagg;
+            if (tot_len != total) fail = true;
+            if (!fail) {
+                const long long pad = total % plen != 0;
+                const long long num_segs = rows + nd - 1 - tot_al + pad;
+                a.doc_out[nd] = static_cast<int32_t>(total);
+                a.doc_in[nd] = static_cast<int32_t>(total);
+                a.aligned[nd] = static_cast<int32_t>(tot_al);
+                *a.num_segs = static_cast<int32_t>(num_segs);
+                a.row_seg_ptr[rows] = static_cast<int32_t>(num_segs);
+                a.cu_seqlens[num_segs] = static_cast<int32_t>(rows * plen);
+            }
+        }
+        if (fail) {
+            set_status(a.status, kErrBadDocs);
+            *a.num_segs = 0;
+        }
+    }
 }
 
 // First index d in [lo, hi) with a[d] >= x (hi if none); a strictly increasing.
@@ -148,88 +295,41 @@ __global__ void __launch_bounds__(kScanThreads) pack_scan_kernel(PackArgs a, int
     }
     __syncthreads();
 
+    // build_unpack (build_pack runs pack_prefix_kernel instead)
     int num_segs;
-    if (a.packed) {
-        // The document offsets are read many times below (every row's binary
-        // search among them): from shared memory when they fit.
-        __shared__ int32_t s_in[kScanSmemDocs];
-        const bool in_smem = nd + 1 <= kScanSmemDocs;
-        if (in_smem) {
-            for (int d = tid; d <= nd; d += kScanThreads) s_in[d] = a.doc_in[d];
-            __syncthreads();
-        }
-        const int32_t *din = in_smem ? s_in : a.doc_in;
-        // Segment boundaries are the union of document starts, row starts and
-        // the padding start. A document start that falls on a row start is
-        // the same boundary; count those ("aligned") so ranks stay exact.
-        long long carry_al = 0;
-        for (int base = 0; base < nd; base += kScanThreads) {
-            int d = base + tid;
-            int flag = (d >= 1 && d < nd && (din[d] % plen) == 0) ? 1 : 0;
-            long long tot;
-            long long e = block_excl_scan(flag, &tot, sh) + carry_al;
-            if (d < nd) aux[d] = static_cast<int32_t>(e);  // aligned starts before d
-            carry_al += tot;
-        }
-        if (tid == 0) aux[nd] = static_cast<int32_t>(carry_al);
-        __syncthreads();
-        const long long total = a.num_tokens;
-        const int pad = (total % plen) != 0;
-        num_segs = a.rows == 0 ? 0 : static_cast<int>(a.rows + nd - 1 - aux[nd] + pad);
-        for (int d = tid; d < nd; d += kScanThreads) {
-            long long s = din[d];
-            a.doc_out[d] = static_cast<int32_t>(s);
-            if (d >= 1 && (s % plen) != 0) {
-                long long rank = (s - 1) / plen + d - aux[d];
-                a.cu_seqlens[rank] = static_cast<int32_t>(s);
-            }
-        }
-        if (tid == 0) a.doc_out[nd] = static_cast<int32_t>(total);
-        for (int r = tid; r <= a.rows; r += kScanThreads) {
-            long long rank = 0;
-            if (r > 0) {
-                int ds = lower_bound(din, 0, nd, r * plen);
-                rank = r + ds - 1 - aux[ds] + ((r == a.rows && pad) ? 1 : 0);
-            }
-            a.cu_seqlens[rank] = static_cast<int32_t>(r * plen);
-            a.row_seg_ptr[r] = static_cast<int32_t>(rank);
-        }
-        if (tid == 0 && pad) a.cu_seqlens[num_segs - 1] = static_cast<int32_t>(total);
-    } else {
-        // One segment per kept document, plus a padding segment in every row
-        // that the kept documents do not fill.
-        const int mb = a.micro_bsz;
-        long long carry_pad = 0;
-        for (int base = 0; base < a.rows; base += kScanThreads) {
-            int r = base + tid;
-            int flag = 0;
-            if (r < a.rows) {
-                int d0 = r * mb, d1 = min(nd, d0 + mb);
-                long long fill = static_cast<long long>(aux[d1]) - aux[d0];
-                flag = fill < plen ? 1 : 0;
-            }
-            long long tot;
-            long long e = block_excl_scan(flag, &tot, sh) + carry_pad;
-            if (r < a.rows) a.row_seg_ptr[r] = static_cast<int32_t>(static_cast<long long>(r) * mb + e);
-            carry_pad += tot;
-        }
-        num_segs = static_cast<int>(nd + carry_pad);
-        if (tid == 0) a.row_seg_ptr[a.rows] = num_segs;
-        __syncthreads();
-        for (int d = tid; d < nd; d += kScanThreads) {
-            int r = d / mb;
-            long long out = r * plen + aux[d] - aux[r * mb];
-            a.doc_out[d] = static_cast<int32_t>(out);
-            a.cu_seqlens[a.row_seg_ptr[r] + (d - r * mb)] = static_cast<int32_t>(out);
-        }
-        for (int r = tid; r < a.rows; r += kScanThreads) {
+    // One segment per kept document, plus a padding segment in every row
+    // that the kept documents do not fill.
+    const int mb = a.micro_bsz;
+    long long carry_pad = 0;
+    for (int base = 0; base < a.rows; base += kScanThreads) {
+        int r = base + tid;
+        int flag = 0;
+        if (r < a.rows) {
             int d0 = r * mb, d1 = min(nd, d0 + mb);
             long long fill = static_cast<long long>(aux[d1]) - aux[d0];
-            if (fill < plen)
-                a.cu_seqlens[a.row_seg_ptr[r] + (d1 - d0)] = static_cast<int32_t>(r * plen + fill);
+            flag = fill < plen ? 1 : 0;
         }
-        if (tid == 0) a.cu_seqlens[num_segs] = static_cast<int32_t>(a.rows * plen);
+        long long tot;
+        long long e = block_excl_scan(flag, &tot, sh) + carry_pad;
+        if (r < a.rows) a.row_seg_ptr[r] = static_cast<int32_t>(static_cast<long long>(r) * mb + e);
+        carry_pad += tot;
     }
+    num_segs = static_cast<int>(nd + carry_pad);
+    if (tid == 0) a.row_seg_ptr[a.rows] = num_segs;
+    __syncthreads();
+    for (int d = tid; d < nd; d += kScanThreads) {
+        int r = d / mb;
+        long long out = r * plen + aux[d] - aux[r * mb];
+        a.doc_out[d] = static_cast<int32_t>(out);
+        a.cu_seqlens[a.row_seg_ptr[r] + (d - r * mb)] = static_cast<int32_t>(out);
+    }
+    for (int r = tid; r < a.rows; r += kScanThreads) {
+        int d0 = r * mb, d1 = min(nd, d0 + mb);
+        long long fill = static_cast<long long>(aux[d1]) - aux[d0];
+        if (fill < plen)
+            a.cu_seqlens[a.row_seg_ptr[r] + (d1 - d0)] = static_cast<int32_t>(r * plen + fill);
+    }
+    if (tid == 0) a.cu_seqlens[num_segs] = static_cast<int32_t>(a.rows * plen);
     if (tid == 0) *a.num_segs = num_segs;
     __syncthreads();
     for (int i = tid; i < num_segs; i += kScanThreads) {
@@ -470,6 +570,52 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
             }
         }
     }
+
+    // Segment fields of the boundaries inside this chunk: document starts not on
+    // a row start, row starts and the padding start. A boundary's place in
+    // cu_seqlens follows from the counts the prefix kernel wrote: before a
+    // document start s (document d) lie the row starts up to s and the
+    // documents 1 .. d - 1 that do not start on a row start; before a row start
+    // r * plen, r row starts and the documents 1 .. ds - 1 (ds the first
+    // document starting at or after it) less the ones on a row start. Each
+    // segment's length goes to its row's max_seqlen (zeroed by the prefix kernel).
+    const int rows = a.rows;
+    auto doc_start = [&](int d) -> int {
+        const int i = d - d_lo;
+        return (i >= 0 && i < W) ? s_doc[i] : a.doc_out[d];
+    };
+    if (P0 < total) {
+        for (int d = d_lo + tid; d < nd; d += kStreamThreads) {
+            const int st = doc_start(d);
+            if (st >= P1) break;
+            if (st < P0 || st % plen == 0) continue;   // on a row start: the row's boundary below
+            const int row = st / plen;
+            const int end = min(doc_start(d + 1), (row + 1) * plen);
+            a.cu_seqlens[(st - 1) / plen + d - a.aligned[d]] = st;
+            atomicMax(&a.max_seqlen[row], end - st);
+        }
+    }
+    for (long long r = (static_cast<long long>(P0) + plen - 1) / plen + tid; r < rows; r += kStreamThreads) {
+        const int x = static_cast<int>(r * plen);   // < rows * plen <= 2^31 - 65537
+        if (x >= P1) break;
+        const int ds = lower_bound(a.doc_out, 0, nd, x);   // first document starting at or after x
+        const int rank = r == 0 ? 0 : static_cast<int>(r) + ds - 1 - a.aligned[ds];
+        a.cu_seqlens[rank] = x;
+        a.row_seg_ptr[r] = rank;
+        // the segment from x ends at the next document start, the row end or num_tokens
+        int next = x + plen;
+        if (ds < nd) {
+            const int sd = a.doc_out[ds];
+            next = min(next, sd == x ? a.doc_out[ds + 1] : sd);
+        } else {
+            next = min(next, total);
+        }
+        atomicMax(&a.max_seqlen[r], next - x);
+    }
+    if (tid == 0 && total % plen != 0 && P0 <= total && total < P1) {   // the padding tail of the last row
+        a.cu_seqlens[*a.num_segs - 1] = total;
+        atomicMax(&a.max_seqlen[total / plen], rows * plen - total);
+    }
 }
 
 // At most 32 registers per thread (8 resident CTAs per SM): the 1025 CTAs of a
@@ -641,8 +787,11 @@ __global__ void __launch_bounds__(kFusedThreads, 8) pack_fused_kernel(PackArgs a
 
 size_t pack_ws_bytes(int64_t num_docs)
 {
-    // status header + 4 arrays of num_docs + 1 int32
-    return kWsHeader + 4 * align_up(sizeof(int32_t) * static_cast<size_t>(num_docs + 1), 256);
+    // status header + 4 arrays of num_docs + 1 int32 + the prefix kernel's CTA
+    // ticket and look-back descriptors (two per CTA)
+    const size_t nb = static_cast<size_t>((num_docs + kPrefixDocs - 1) / kPrefixDocs);
+    return kWsHeader + 4 * align_up(sizeof(int32_t) * static_cast<size_t>(num_docs + 1), 256) +
+           align_up(8 + 16 * (nb > 0 ? nb : 1), 256);
 }
 
 cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
@@ -655,6 +804,9 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
     a.doc_in = reinterpret_cast<int32_t *>(ws + kWsHeader + arr);
     a.doc_keep = reinterpret_cast<int32_t *>(ws + kWsHeader + 2 * arr);
     int32_t *aux = reinterpret_cast<int32_t *>(ws + kWsHeader + 3 * arr);
+    a.aligned = aux;
+    a.ticket = reinterpret_cast<unsigned *>(ws + kWsHeader + 4 * arr);
+    a.look = reinterpret_cast<unsigned long long *>(ws + kWsHeader + 4 * arr + 8);
 
     const long long npos = static_cast<long long>(a.rows) * a.plen;
     if (a.packed && a.num_docs >= 1 && a.num_docs <= kFusedDocs && a.rows <= kFusedRows) {
@@ -672,8 +824,21 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
         prof_end(kProfPackStream, stream);
         return e0;
     }
-    pack_scan_kernel<<<1, kScanThreads, 0, stream>>>(a, aux);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (a.packed) {
+        const int nb = static_cast<int>((static_cast<long long>(a.num_docs) + kPrefixDocs - 1) / kPrefixDocs);
+        if (nb > 1) {
+            // several CTAs chain their prefixes: clear the status word, the ticket
+            // and the look-back descriptors first
+            if ((e = cudaMemsetAsync(a.status, 0, sizeof(int), stream)) != cudaSuccess) return e;
+            if ((e = cudaMemsetAsync(a.ticket, 0, 8 + 16 * static_cast<size_t>(nb), stream)) != cudaSuccess)
+                return e;
+        }
+        pack_prefix_kernel<<<static_cast<unsigned>(nb > 0 ? nb : 1), kScanThreads, 0, stream>>>(a, nb > 0 ? nb : 1);
+    } else {
+        pack_scan_kernel<<<1, kScanThreads, 0, stream>>>(a, aux);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (npos == 0) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};

@@ -200,3 +200,38 @@ def test_bad_doc_lengths_set_status(ops):
     assert st == -7
     st, g = _gpu_pack(ops, toks.cpu().numpy(), [4, 6], 2, 4, True)      # and the next call is clean
     assert st == 0 and g["num_segs"] == 4 and g["cu_seqlens"].tolist() == [0, 4, 8, 10, 16]
+
+
+@pytest.mark.parametrize("n_docs,len_hi,mb,sl", [
+    (40000, 8, 1, 65536),        # 10 prefix CTAs chained by the look-back
+    (300000, 8, 4, 8192),        # 74 prefix CTAs, many rows, documents split across rows
+    (9000, 3000, 2, 4096),       # 3 prefix CTAs, long documents over many rows, a padding tail
+])
+def test_many_documents_multi_cta_prefix(ops, n_docs, len_hi, mb, sl):
+    """build_pack with more than 4096 documents: the document-start prefix and
+    the aligned-start counts are chained across CTAs (decoupled look-back); the
+    segment fields come from the stream kernel. Bit-exact against the C oracle
+    twin (itself pinned to the literal oracle)."""
+    rng = np.random.default_rng(n_docs)
+    lens = rng.integers(1, len_hi + 1, size=n_docs).astype(np.int32)
+    toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+    st, g = _gpu_pack(ops, toks, lens, mb, sl, True)
+    assert st == 0
+    _assert_same(g, OA.pack(toks, lens, mb, sl, True))
+
+
+def test_many_documents_bad_length_sets_status(ops):
+    """A zero-length document in a late prefix CTA and a wrong total are both
+    reported, and the next call on a fresh workspace is clean."""
+    rng = np.random.default_rng(3)
+    lens = rng.integers(1, 9, size=20000).astype(np.int32)
+    toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+    bad = lens.copy()
+    bad[9000] = 0                                              # in the third of five prefix CTAs
+    st, _ = _gpu_pack(ops, toks[:int(bad.sum())], bad, 2, 4096, True)
+    assert st == -7
+    st, _ = _gpu_pack(ops, toks[:-1], lens, 2, 4096, True)          # lengths sum past num_tokens
+    assert st == -7
+    st, g = _gpu_pack(ops, toks, lens, 2, 4096, True)
+    assert st == 0
+    _assert_same(g, OA.pack(toks, lens, 2, 4096, True))
