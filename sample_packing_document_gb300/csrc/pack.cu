@@ -72,43 +72,53 @@ __device__ long long block_excl_scan(long long v, long long *total, long long *s
 // ---------------------------------------------------------------- build_pack prefix
 constexpr int kPrefixDocs = kScanThreads * kScanItems;   // documents per prefix CTA
 
-// Decoupled look-back over the prefix CTAs (thread 0 of each): publish this
-// CTA's aggregate, add up the predecessors' published values back to the
-// first inclusive one, publish the inclusive prefix. A CTA only waits on CTAs
-// that took their order ticket earlier, which are running, so the chain ends;
-// the wait is bounded all the same (status SPD_ERR_DEVICE_TIMEOUT). Values are
-// clamped below 2^40 (valid inputs stay below 2^31).
+// Decoupled look-back over the prefix CTAs, by one warp of each: publish this
+// CTA's aggregate, then read the predecessors' published words 32 at a time
+// (lane l reads CTA bid - 1 - l - 32 k), adding up aggregates back to the
+// nearest inclusive prefix; publish the inclusive prefix. A CTA only waits on
+// CTAs that took their order ticket earlier, which are running, so the chain
+// ends; the wait is bounded all the same (status SPD_ERR_DEVICE_TIMEOUT).
+// Values are clamped below 2^40 (valid inputs stay below 2^31). Returns the
+// exclusive prefix in every lane.
 __device__ long long lookback_excl(unsigned long long *look, int bid, long long agg, int *status)
 {
     constexpr unsigned long long kAgg = 1ull << 62, kInc = 2ull << 62, kVal = (1ull << 62) - 1;
-    const unsigned long long v = static_cast<unsigned long long>(agg < (1LL << 40) ? agg : (1LL << 40));
+    constexpr long long kCap = 1LL << 40;
+    const int lane = threadIdx.x & 31;
+    const unsigned long long v = static_cast<unsigned long long>(agg < kCap ? agg : kCap);
     if (bid == 0) {
-        st_release_u64(look, kInc | v);
+        if (lane == 0) st_release_u64(look, kInc | v);
         return 0;
     }
-    st_release_u64(look + bid, kAgg | v);
+    if (lane == 0) st_release_u64(look + bid, kAgg | v);
     long long excl = 0;
-    int j = bid - 1;
+    int base = bid - 1;
     const uint64_t t0 = globaltimer_ns();
-    while (j >= 0) {
-        const unsigned long long w = ld_acquire_u64(look + j);
+    while (true) {
+        const int j = base - lane;
+        // before CTA 0 nothing is added: read as an inclusive zero
+        const unsigned long long w = j >= 0 ? ld_acquire_u64(look + j) : kInc;
         const unsigned long long state = w >> 62;
-        if (state == 2) {
-            excl += static_cast<long long>(w & kVal);
-            break;
-        }
-        if (state == 1) {
-            excl += static_cast<long long>(w & kVal);
-            --j;
+        const unsigned inc = __ballot_sync(0xffffffffu, state == 2);
+        const unsigned empty = __ballot_sync(0xffffffffu, state == 0);
+        const int first = inc ? __ffs(inc) - 1 : 32;   // nearest inclusive prefix in the window
+        const unsigned needed = first == 32 ? 0xffffffffu : (first == 31 ? 0xffffffffu : (2u << first) - 1u);
+        if (empty & needed) {                          // a predecessor has not published yet
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                if (lane == 0) set_status(status, kErrTimeout);
+                break;
+            }
             continue;
         }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            set_status(status, kErrTimeout);
-            break;
-        }
+        long long x = lane <= first ? static_cast<long long>(w & kVal) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        excl += x;
+        if (first < 32) break;
+        base -= 32;
     }
-    const long long inc = excl + static_cast<long long>(v);
-    st_release_u64(look + bid, kInc | static_cast<unsigned long long>(inc < (1LL << 40) ? inc : (1LL << 40)));
+    const long long incl = excl + static_cast<long long>(v);
+    if (lane == 0) st_release_u64(look + bid, kInc | static_cast<unsigned long long>(incl < kCap ? incl : kCap));
     return excl;
 }
 
@@ -148,7 +158,10 @@ __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, i
     }
     long long agg;
     const long long e = block_excl_scan(sum, &agg, sh);
-    if (tid == 0) s_excl[0] = lookback_excl(a.look, bid, agg, a.status);
+    if (tid < 32) {
+        const long long x = lookback_excl(a.look, bid, agg, a.status);
+        if (tid == 0) s_excl[0] = x;
+    }
     __syncthreads();
     long long start[kScanItems];
     long long run = s_excl[0] + e;
@@ -168,7 +181,10 @@ __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, i
     }
     long long fagg;
     const long long fe = block_excl_scan(fsum, &fagg, sh);
-    if (tid == 0) s_excl[1] = lookback_excl(a.look + nb, bid, fagg, a.status);
+    if (tid < 32) {
+        const long long x = lookback_excl(a.look + nb, bid, fagg, a.status);
+        if (tid == 0) s_excl[1] = x;
+    }
     __syncthreads();
     long long frun = s_excl[1] + fe;
 #pragma unroll
@@ -466,6 +482,7 @@ constexpr int kWin = 1024;   // document starts staged per CTA
 __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(PackArgs a)
 {
     __shared__ int32_t s_doc[kWin];
+    __shared__ int32_t s_max[kWin];   // per-row maxima of this chunk's segments
     const int tid = threadIdx.x, lane = tid & 31;
     const int total = a.num_tokens, nd = a.num_docs, plen = a.plen;
     const int npos = a.rows * plen;   // rows * plen <= 2^31 - 1 is checked on the host
@@ -584,6 +601,20 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
         const int i = d - d_lo;
         return (i >= 0 && i < W) ? s_doc[i] : a.doc_out[d];
     };
+    // Per-row maxima of this chunk's segments are first combined in shared
+    // memory (a chunk of very short documents holds hundreds of segments of
+    // one row; one global atomic each would queue on one address), then added
+    // with one global atomic per row. Chunks spanning more rows than the
+    // staging holds use global atomics directly.
+    const int row0 = P0 / plen;
+    const int nrow = (P1 - 1) / plen - row0 + 1;
+    const bool smem_max = nrow <= kWin;
+    for (int i = tid; i < nrow && smem_max; i += kStreamThreads) s_max[i] = 0;
+    __syncthreads();
+    auto seg_max = [&](int row, int len) {
+        if (smem_max) atomicMax(&s_max[row - row0], len);
+        else atomicMax(&a.max_seqlen[row], len);
+    };
     if (P0 < total) {
         for (int d = d_lo + tid; d < nd; d += kStreamThreads) {
             const int st = doc_start(d);
@@ -592,7 +623,7 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
             const int row = st / plen;
             const int end = min(doc_start(d + 1), (row + 1) * plen);
             a.cu_seqlens[(st - 1) / plen + d - a.aligned[d]] = st;
-            atomicMax(&a.max_seqlen[row], end - st);
+            seg_max(row, end - st);
         }
     }
     for (long long r = (static_cast<long long>(P0) + plen - 1) / plen + tid; r < rows; r += kStreamThreads) {
@@ -610,11 +641,16 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
         } else {
             next = min(next, total);
         }
-        atomicMax(&a.max_seqlen[r], next - x);
+        seg_max(static_cast<int>(r), next - x);
     }
     if (tid == 0 && total % plen != 0 && P0 <= total && total < P1) {   // the padding tail of the last row
         a.cu_seqlens[*a.num_segs - 1] = total;
-        atomicMax(&a.max_seqlen[total / plen], rows * plen - total);
+        seg_max(total / plen, rows * plen - total);
+    }
+    if (smem_max) {
+        __syncthreads();
+        for (int i = tid; i < nrow; i += kStreamThreads)
+            if (s_max[i] > 0) atomicMax(&a.max_seqlen[row0 + i], s_max[i]);
     }
 }
 
