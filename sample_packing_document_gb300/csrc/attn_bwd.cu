@@ -57,7 +57,7 @@ constexpr uint32_t kPRegs = 112, kDsRegs = 104, kControlRegs = 48;
 constexpr int kPWarps = 8, kDsWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAtom = 128 * 128;
-constexpr int kQStages = 2;
+constexpr int kQStages = 2;   // the per-stage counters below are selected with (index & 1)
 
 template <int D>
 struct BwdSmem {
@@ -371,12 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                 if (u > 0 && !mbar_wait(&sm.q_empty[st], (u - 1) & 1, abort_flag, a.status)) return false;
                 mbar_arrive_expect_tx(&sm.q_full[st], kTileBytes);
                 for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.q[st][c], &a.tm_q, c * 64, h, q0, &sm.q_full[st]);
-                last_q[st] = u;
+                if (st) last_q[1] = u;   // constant indices keep the arrays in registers
+                else last_q[0] = u;
                 if (u > 0 && !mbar_wait(&sm.do_empty[st], (u - 1) & 1, abort_flag, a.status)) return false;
                 mbar_arrive_expect_tx(&sm.do_full[st], kTileBytes);
                 for (int c = 0; c < D / 64; ++c)
                     tma_load_3d(sm.dout[st][c], &a.tm_do, c * 64, h, q0, &sm.do_full[st]);
-                last_do[st] = u;
+                if (st) last_do[1] = u;
+                else last_do[0] = u;
                 return true;
             };
             bool ok = true;
@@ -508,7 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_kernel(const __grid_cons
                                               kk * (2048 >> 4), id_kn, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(&sm.do_empty[st]);
-                    ++do_commits[st];
+                    if (st) ++do_commits[1];   // constant indices keep the counts in registers
+                    else ++do_commits[0];
                     // dK += dS^T Q (M = kv), dQ_part = dS K (M = q) into B
                     if (!mbar_wait(&sm.ds_full, ph, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();

@@ -40,7 +40,7 @@
 namespace spd {
 namespace {
 
-constexpr int kStages = 2;
+constexpr int kStages = 2;   // the per-stage counters below are selected with (index & 1)
 constexpr int kThreads = 384;
 // Register split (setmaxnreg): the launch gives 168 per thread (384 x 168 = 64512);
 // the warpgroup of the producer / MMA issuer drops to 72 and the two softmax
@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (use > 0 && !mbar_wait(&sm.v_empty[st], (use - 1) & 1, abort_flag, a.status)) return false;
                 mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
                 for (int c = 0; c < D / 64; ++c) tma_load_3d(sm.v[st][c], &a.tm_v, c * 64, g, row, &sm.v_full[st]);
-                last_v_use[st] = use;
+                if (st) last_v_use[1] = use;   // constant indices keep the array in registers
+                else last_v_use[0] = use;
                 return true;
             };
             for (int it = 0;; ++it) {
@@ -215,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
                     for (int c = 0; c < D / 64; ++c)
                         tma_load_3d(sm.k[st][c], &a.tm_k, c * 64, g, kv0, &sm.k_full[st]);
-                    last_k_use[st] = use;
+                    if (st) last_k_use[1] = use;
+                    else last_k_use[0] = use;
                     if (pend_v >= 0 && !load_v(pend_v, pend_row, pend_g)) { ok = false; break; }
                     pend_v = static_cast<int>(kv_iter);
                     pend_row = kv0;
@@ -284,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 issue_s(0, 0);                        // S regions: the last P V of each tile ran before
                 if (n_tile1 > 0) issue_s(1, 0);
                 umma_commit(&sm.k_empty[kv_iter % kStages]);   // K(0) read by both tiles' first S
-                ++k_commits[kv_iter % kStages];
+                if (kv_iter % kStages) ++k_commits[1];   // constant indices keep the counts in registers
+                else ++k_commits[0];
                 for (int j = 0; ok && j < us.n_kv; ++j) {
                     const uint32_t kvj = kv_iter + j;
                     const int st = kvj % kStages;
@@ -321,10 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     if (!ok) break;
                     if (next_k) {                     // K(j + 1) read by every S of this step
                         umma_commit(&sm.k_empty[(kvj + 1) % kStages]);
-                        ++k_commits[(kvj + 1) % kStages];
+                        if ((kvj + 1) % kStages) ++k_commits[1];
+                        else ++k_commits[0];
                     }
                     umma_commit(&sm.v_empty[st]);     // V(j) read by every P V of this step
-                    ++v_commits[st];
+                    if (st) ++v_commits[1];
+                    else ++v_commits[0];
                 }
                 kv_iter += us.n_kv;
             }
