@@ -975,9 +975,12 @@ def e2e_measure(args, ops, w, toks, lens, dev, step_ms=0.0):
     for kk in range(2 * NB):
         step(kk)
     torch.cuda.synchronize()
-    # a window long enough that one fill and one drain (the first step's copies
-    # in, the last one's copies out) weigh little per step
-    n = max(24 if step_ms < 50.0 else 8, args.steps)
+    # A window long enough that one fill and one drain (the first step's copies
+    # in, the last ones' copies out) weigh little per step. While the attention
+    # kernels run, the copy engines move data far below their idle rate (a
+    # 3.2 GB read-back took 58-228 ms instead of 17), so the drain after the
+    # last step is long.
+    n = max(24, args.steps)
     a, bev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         time.sleep(0.5)                           # nvidia-smi has started sampling
