@@ -684,6 +684,27 @@ def data_measure(ops, dev, reps=20):
     out["pad_for_sequence_parallel"] = {"workload": "labels row of %d tokens padded to %d (sp_size %d)" % (
         T, padded, sp), "ms": ms, "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9,
         "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    # the same two steps on 16 rows of the c5 row's length (a size at which the launch no longer
+    # dominates): sequence split of three [16, 1048576] tensors, padding of a [16, 1048573] labels tensor
+    rows16 = 16
+    T = 1 << 20
+    src = [torch.randint(0, 50000, (rows16, T), dtype=torch.int32, device=dev) for _ in range(3)]
+    dst = [torch.empty((rows16, T // sp), dtype=torch.int32, device=dev) for _ in range(3)]
+    ms = _time_kernel(ops, ops.PROFILE_SPLIT, lambda: ops.split_sequence_parallel(src, sp, 3, out=dst), flush, reps)
+    nbytes = 3 * 2 * 4 * rows16 * (T // sp)
+    out["split_sequence_parallel_16_rows"] = {
+        "workload": "16 rows of %d tokens (three tensors), sp_size %d, rank 3" % (T, sp), "ms": ms, "bytes": nbytes,
+        "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    del src, dst
+    T = (1 << 20) - 3
+    lab = torch.randint(-100, 50000, (rows16, T), dtype=torch.int32, device=dev)
+    ms = _time_kernel(ops, ops.PROFILE_PAD, lambda: ops.pad_for_sequence_parallel(sp, labels=lab), flush, reps)
+    padded = -(-T // sp) * sp
+    nbytes = rows16 * (4 * T + 4 * padded)
+    out["pad_for_sequence_parallel_16_rows"] = {
+        "workload": "16 labels rows of %d tokens padded to %d (sp_size %d)" % (T, padded, sp), "ms": ms,
+        "bytes": nbytes, "GB/s": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+    del lab
     # RoPE in place on the c2 batch's q and k (32 + 32 heads x 32768 tokens x 128), positions restarting
     # at every document (the library's pack of the c2 documents gives them as indexes)
     w, lens, toks = workload_docs("c2")
