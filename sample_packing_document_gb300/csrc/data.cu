@@ -70,25 +70,45 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a)
     const int32_t chunk = a.len / a.sp_size;
     const int32_t total = a.rows * chunk;
     const int32_t off = a.rank * chunk;
-    // 64-bit loop index: the step past the last group must not wrap (total < 2^31)
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads * 4;
+    // Two groups of four positions per thread and iteration, every load issued
+    // before the first store (up to six 16-byte loads in flight per thread).
+    // 64-bit loop index: the step past the last group must not wrap (total < 2^31).
     for (int64_t xl = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * 4; xl < total;
-         xl += static_cast<int64_t>(gridDim.x) * kThreads * 4) {
-        const int32_t x = static_cast<int32_t>(xl);
-        const int32_t r = x / chunk, j = x - r * chunk;
-        const int32_t src = r * a.len + off + j;
+         xl += 2 * stride) {
+        int32_t x[2], src[2];
+        bool full[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t xu = xl + u * stride;
+            x[u] = xu < total ? static_cast<int32_t>(xu) : total;
+            const int32_t r = x[u] / chunk, j = x[u] - r * chunk;
+            src[u] = r * a.len + off + j;
+            full[u] = a.vec && x[u] + 4 <= total;   // chunk % 4 == 0: the group stays in one row
+        }
+        int4 v[2][3];
         // unrolled over the (at most three) tensors so that the pointer arrays are
         // indexed with constants and stay in the parameter space
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
-            if (t >= a.n_tensors) break;
-            if (a.vec && x + 4 <= total) {   // chunk % 4 == 0: the group stays in one row
-                *reinterpret_cast<int4 *>(a.dst[t] + x) = *reinterpret_cast<const int4 *>(a.src[t] + src);
-            } else {
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if (x + k >= total) break;
-                    const int32_t rr = (x + k) / chunk, jj = (x + k) - rr * chunk;
-                    a.dst[t][x + k] = a.src[t][rr * a.len + off + jj];
+            for (int t = 0; t < 3; ++t)
+                if (t < a.n_tensors && full[u]) v[u][t] = *reinterpret_cast<const int4 *>(a.src[t] + src[u]);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (x[u] >= total) continue;
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                if (t >= a.n_tensors) break;
+                if (full[u]) {
+                    *reinterpret_cast<int4 *>(a.dst[t] + x[u]) = v[u][t];
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (x[u] + k >= total) break;
+                        const int32_t rr = (x[u] + k) / chunk, jj = (x[u] + k) - rr * chunk;
+                        a.dst[t][x[u] + k] = a.src[t][rr * a.len + off + jj];
+                    }
                 }
             }
         }
@@ -101,27 +121,45 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a)
 __global__ void __launch_bounds__(kThreads) pad_kernel(PadArgs a)
 {
     const int32_t total = a.rows * a.padded;
-    // 64-bit loop index: the step past the last group must not wrap (total < 2^31)
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads * 4;
+    // Two groups of four output positions per thread and iteration, all eight
+    // loads issued before the stores. 64-bit loop index: the step past the last
+    // group must not wrap (total < 2^31).
     for (int64_t xl = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * 4; xl < total;
-         xl += static_cast<int64_t>(gridDim.x) * kThreads * 4) {
-        const int32_t x = static_cast<int32_t>(xl);
-        int32_t v[4];
+         xl += 2 * stride) {
+        int32_t v[2][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int32_t q = x + k;
-            if (q >= total) {
-                v[k] = 0;
-                continue;
+        for (int u = 0; u < 2; ++u) {
+            const int64_t xu = xl + u * stride;
+            // the row of the group's first position; a group crosses at most into the next row
+            const int32_t x = xu < total ? static_cast<int32_t>(xu) : total;
+            int32_t r = x / a.padded, j = x - r * a.padded;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int32_t q = x + k;
+                if (k > 0 && ++j == a.padded) {
+                    j = 0;
+                    ++r;
+                }
+                if (q >= total) {
+                    v[u][k] = 0;
+                    continue;
+                }
+                v[u][k] = j < a.len ? a.src[static_cast<int64_t>(r) * a.len + j] : (a.count ? j - a.len : a.value);
             }
-            const int32_t r = q / a.padded, j = q - r * a.padded;
-            v[k] = j < a.len ? a.src[static_cast<int64_t>(r) * a.len + j] : (a.count ? j - a.len : a.value);
         }
-        if (a.vec && x + 4 <= total) {
-            *reinterpret_cast<int4 *>(a.dst + x) = make_int4(v[0], v[1], v[2], v[3]);
-        } else {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (x + k < total) a.dst[x + k] = v[k];
+        for (int u = 0; u < 2; ++u) {
+            const int64_t xu = xl + u * stride;
+            if (xu >= total) continue;
+            const int32_t x = static_cast<int32_t>(xu);
+            if (a.vec && x + 4 <= total) {
+                *reinterpret_cast<int4 *>(a.dst + x) = make_int4(v[u][0], v[u][1], v[u][2], v[u][3]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (x + k < total) a.dst[x + k] = v[u][k];
+            }
         }
     }
 }
