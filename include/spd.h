@@ -20,7 +20,10 @@
  * and the data steps that follow packing (page "Data loading and flow",
  * section "Processing data"): spd_unpack_data and
  * spd_split_sequence_parallel, and the sequence-parallel padding before the
- * split (spd_pad_for_sequence_parallel).
+ * split (spd_pad_for_sequence_parallel); the steps next to attention: rotary
+ * position embedding with per-document positions (spd_rope, and fused into
+ * the forward's prologue: spd_varlen_attn_fwd_rope) and the masked token loss
+ * over the packed labels (spd_masked_token_loss).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
