@@ -727,6 +727,8 @@ __global__ void __launch_bounds__(kFusedThreads, 8) pack_fused_kernel(PackArgs a
     if (blockIdx.x > 0 && p < npos) {
         int32_t id[4], lab[4], idx[4];
         int d = p < total ? last_le_smem(s_start, nd, p) : 0;
+        int start = s_start[d], end = s_start[d + 1];   // document d (s_start[nd] = total)
+        int row_start = p - p % plen;                    // one division per thread
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int q = p + k;
@@ -737,11 +739,15 @@ __global__ void __launch_bounds__(kFusedThreads, 8) pack_fused_kernel(PackArgs a
                 idx[k] = q - total;
                 continue;
             }
-            while (d + 1 < nd && s_start[d + 1] <= q) ++d;
-            const int start = s_start[d], end = s_start[d + 1];
+            if (q >= end) {                              // the next document(s)
+                do ++d;
+                while (s_start[d + 1] <= q);
+                start = s_start[d];
+                end = s_start[d + 1];
+            }
+            while (q >= row_start + plen) row_start += plen;
             id[k] = tk[k];
             lab[k] = (q + 1 < end) ? tk[k + 1] : -100;
-            const int row_start = (q / plen) * plen;
             idx[k] = q - (start > row_start ? start : row_start);
         }
         if (a.vec_out && p + 4 <= npos) {
