@@ -201,16 +201,15 @@ static int attn_fwd_impl(const uint16_t *q, const uint16_t *k, const uint16_t *v
     a.debug_skip = take_debug_skip(SPD_DEBUG_SKIP_FWD_Q);
     a.rope = rope;
     if (rope) {
-        const double base = rope_theta > 0.f ? static_cast<double>(rope_theta) : 10000.0;
+        const double theta = rope_theta > 0.f ? static_cast<double>(rope_theta) : 10000.0;
         for (int j = 0; j < head_dim / 2; ++j) {
             // turns per position, theta_j / (2 pi) < 1/6, as 64-bit fixed point
-            const double turns = std::pow(base, -2.0 * j / head_dim) / (2.0 * 3.141592653589793238462643);
+            const double turns = std::pow(theta, -2.0 * j / head_dim) / (2.0 * 3.141592653589793238462643);
             a.freq[j] = static_cast<unsigned long long>(std::ldexp(turns, 64));
         }
     }
     return cuda_rc(launch_attn_fwd(a, head_dim, (total_tokens + 2 * kTile - 1) / (2 * kTile) + num_segs, s));
 }
-
 
 extern "C" {
 
