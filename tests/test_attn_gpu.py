@@ -96,8 +96,13 @@ def test_small_cases_full_compare(ops, lens, Hq, Hkv, d):
     _check_full(ops, lens, Hq, Hkv, d, seed=sum(lens) % 97)
 
 
-def test_bf16_gradient_output(ops):
-    _check_full(ops, [400, 77, 900], 4, 4, 128, seed=3, grad_dtype=torch.bfloat16)
+@pytest.mark.parametrize("lens,Hq,Hkv,d", [
+    ([400, 77, 900], 4, 4, 128),
+    ([1, 250, 127, 384, 64], 6, 2, 64),             # head_dim 64 (no TMA-box store of dK / dV), group 3
+    ([700, 33, 1290], 7, 1, 128),                   # group 7
+])
+def test_bf16_gradient_output(ops, lens, Hq, Hkv, d):
+    _check_full(ops, lens, Hq, Hkv, d, seed=3, grad_dtype=torch.bfloat16)
 
 
 def test_custom_scale_and_scaled_q(ops):
