@@ -124,7 +124,11 @@ __device__ long long lookback_excl(unsigned long long *look, int bid, long long 
 
 __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, int nb)
 {
-    // The stream kernel may load its tokens and store input_ids meanwhile.
+    // Launched as a programmatic dependent of whatever precedes it on the
+    // stream: it waits for that grid (and its memory) first, then lets the
+    // stream kernel start, which may load its tokens and store input_ids
+    // meanwhile.
+    pdl_wait();
     pdl_launch_dependents();
     __shared__ long long sh[33];
     __shared__ long long s_excl[2];   // this CTA's exclusive prefix: document starts, aligned starts
@@ -158,9 +162,13 @@ __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, i
     }
     long long agg;
     const long long e = block_excl_scan(sum, &agg, sh);
-    if (tid < 32) {
-        const long long x = lookback_excl(a.look, bid, agg, a.status);
-        if (tid == 0) s_excl[0] = x;
+    if (nb > 1) {   // one CTA: nothing to chain
+        if (tid < 32) {
+            const long long x = lookback_excl(a.look, bid, agg, a.status);
+            if (tid == 0) s_excl[0] = x;
+        }
+    } else if (tid == 0) {
+        s_excl[0] = 0;
     }
     __syncthreads();
     long long start[kScanItems];
@@ -176,14 +184,19 @@ __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, i
 #pragma unroll
     for (int k = 0; k < kScanItems; ++k) {
         const int d = d0 + k;
-        flag[k] = (d >= 1 && d < nd && start[k] % plen == 0) ? 1 : 0;
+        // valid starts are below 2^31 (larger ones fail the length check below)
+        flag[k] = (d >= 1 && d < nd && static_cast<unsigned>(start[k]) % static_cast<unsigned>(plen) == 0) ? 1 : 0;
         fsum += flag[k];
     }
     long long fagg;
     const long long fe = block_excl_scan(fsum, &fagg, sh);
-    if (tid < 32) {
-        const long long x = lookback_excl(a.look + nb, bid, fagg, a.status);
-        if (tid == 0) s_excl[1] = x;
+    if (nb > 1) {
+        if (tid < 32) {
+            const long long x = lookback_excl(a.look + nb, bid, fagg, a.status);
+            if (tid == 0) s_excl[1] = x;
+        }
+    } else if (tid == 0) {
+        s_excl[1] = 0;
     }
     __syncthreads();
     long long frun = s_excl[1] + fe;
@@ -453,7 +466,7 @@ __device__ int block_excl_scan256(int v, int *total, int *sh)
 }
 
 // Largest d in [0, n) with a[d] <= x; assumes a[0] <= x.
-__device__ __forceinline__ int last_le_smem(const int32_t *a, int n, long long x)
+__device__ __forceinline__ int last_le_smem(const int32_t *a, int n, int x)
 {
     int lo = 0, hi = n;
     while (hi - lo > 1) {
@@ -476,10 +489,11 @@ __device__ __forceinline__ int32_t int4_at(const int4 &v, int k)
 // the scan, the CTA finds the document holding its first position with a
 // block-wide search (256 sampled starts per round, one barrier each) and
 // stages the starts of the documents its chunk overlaps in shared memory;
-// labels and indexes then need no global lookups.
+// labels and indexes then need no global lookups. At most 40 registers per
+// thread (6 resident CTAs per SM).
 constexpr int kWin = 1024;   // document starts staged per CTA
 
-__global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(PackArgs a)
+__global__ void __launch_bounds__(kStreamThreads, 6) pack_packed_stream_kernel(PackArgs a)
 {
     __shared__ int32_t s_doc[kWin];
     __shared__ int32_t s_max[kWin];   // per-row maxima of this chunk's segments
@@ -524,8 +538,10 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
     // The document holding position P0 (chunks wholly in the padding need none):
     // doc_out[lo] <= P0 < doc_out[hi] throughout, the range shrinking 256-fold
     // per round.
-    int d_lo = 0, W = 0;
+    __shared__ int s_cnt;
+    int d_lo = 0, W = 0, Wn = 0;
     bool staged = false;
+    if (tid == 0) s_cnt = 0;
     if (P0 < total) {
         int lo = 0, hi = nd;
         while (hi - lo > 1) {
@@ -540,17 +556,37 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
         W = min(kWin, nd + 1 - d_lo);   // doc_out[nd] = num_tokens ends the last document
         for (int i = tid; i < W; i += kStreamThreads) s_doc[i] = a.doc_out[d_lo + i];
         __syncthreads();
-        // staged when the window reaches past the chunk's last token
-        staged = s_doc[W - 1] > min(P1, total) - 1;
+        // staged when the window reaches past the chunk's last token; the
+        // searches then stay inside its first Wn entries (the starts below the
+        // chunk's end and the one after them)
+        const int lim = min(P1, total);
+        staged = s_doc[W - 1] > lim - 1;
+        int c = 0;
+        for (int i = tid; i < W; i += kStreamThreads) c += s_doc[i] < lim;
+        if (c) atomicAdd(&s_cnt, c);
+        __syncthreads();
+        Wn = min(W, s_cnt + 1);
     }
 
+    // The current document's bounds and row are kept across positions: a
+    // search only where a group of four starts past the document, a division
+    // only where it starts past the row.
+    auto doc = [&](int i) -> int { return staged ? s_doc[i] : a.doc_out[d_lo + i]; };
+    int d = 0, start = 0, end = 0, row_start = 0, row_end = 0;
 #pragma unroll
     for (int it = 0; it < kStreamIters; ++it) {
         const int p = P0 + (it * kStreamThreads + tid) * 4;
         if (p >= P1) break;
         int32_t lab[4], idx[4];
-        int d = 0;
-        if (p < total) d = staged ? last_le_smem(s_doc, W, p) : last_le(a.doc_out, d_lo, nd, p) - d_lo;
+        if (p < total && p >= end) {
+            d = staged ? last_le_smem(s_doc, Wn, p) : last_le(a.doc_out, d_lo, nd, p) - d_lo;
+            start = doc(d);
+            end = doc(d + 1);
+        }
+        if (p >= row_end) {
+            row_start = p - p % plen;
+            row_end = row_start + plen;
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int q = p + k;
@@ -559,19 +595,18 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
                 idx[k] = q - total;
                 continue;
             }
-            int start, end;
-            if (staged) {
-                while (s_doc[d + 1] <= q) ++d;   // q < s_doc[W - 1]
-                start = s_doc[d];
-                end = s_doc[d + 1];
-            } else {
-                while (a.doc_out[d_lo + d + 1] <= q) ++d;   // q < doc_out[nd]
-                start = a.doc_out[d_lo + d];
-                end = a.doc_out[d_lo + d + 1];
+            if (q >= end) {     // q < doc_out[nd] = total
+                do ++d;
+                while (doc(d + 1) <= q);
+                start = doc(d);
+                end = doc(d + 1);
+            }
+            if (q >= row_end) {   // q grows by one: at most one row further
+                row_start = row_end;
+                row_end += plen;
             }
             const int next = k < 3 ? int4_at(tk[it], k + 1) : nx[it];
             lab[k] = q + 1 < end ? next : -100;
-            const int row_start = q - q % plen;
             idx[k] = q - (start > row_start ? start : row_start);
         }
         if (a.vec_out && p + 4 <= P1) {
@@ -626,11 +661,14 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
             seg_max(row, end - st);
         }
     }
-    for (long long r = (static_cast<long long>(P0) + plen - 1) / plen + tid; r < rows; r += kStreamThreads) {
-        const int x = static_cast<int>(r * plen);   // < rows * plen <= 2^31 - 65537
+    const int r_first = row0 + (P0 != row0 * plen);   // the first row starting at or after P0
+    for (int r = r_first + tid; r < rows; r += kStreamThreads) {
+        const int x = r * plen;   // < rows * plen <= 2^31 - 65537
         if (x >= P1) break;
-        const int ds = lower_bound(a.doc_out, 0, nd, x);   // first document starting at or after x
-        const int rank = r == 0 ? 0 : static_cast<int>(r) + ds - 1 - a.aligned[ds];
+        // the first document starting at or after x (inside the staged window
+        // when x is a token of this chunk)
+        const int ds = (staged && x < total) ? d_lo + lower_bound(s_doc, 0, Wn, x) : lower_bound(a.doc_out, 0, nd, x);
+        const int rank = r == 0 ? 0 : r + ds - 1 - a.aligned[ds];
         a.cu_seqlens[rank] = x;
         a.row_seg_ptr[r] = rank;
         // the segment from x ends at the next document start, the row end or num_tokens
@@ -641,7 +679,7 @@ __global__ void __launch_bounds__(kStreamThreads) pack_packed_stream_kernel(Pack
         } else {
             next = min(next, total);
         }
-        seg_max(static_cast<int>(r), next - x);
+        seg_max(r, next - x);
     }
     if (tid == 0 && total % plen != 0 && P0 <= total && total < P1) {   // the padding tail of the last row
         a.cu_seqlens[*a.num_segs - 1] = total;
@@ -876,7 +914,16 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
             if ((e = cudaMemsetAsync(a.ticket, 0, 8 + 16 * static_cast<size_t>(nb), stream)) != cudaSuccess)
                 return e;
         }
-        pack_prefix_kernel<<<static_cast<unsigned>(nb > 0 ? nb : 1), kScanThreads, 0, stream>>>(a, nb > 0 ? nb : 1);
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3(static_cast<unsigned>(nb > 0 ? nb : 1));
+        pcfg.blockDim = dim3(kScanThreads);
+        pcfg.stream = stream;
+        cudaLaunchAttribute pattr[1];
+        pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pattr[0].val.programmaticStreamSerializationAllowed = 1;
+        pcfg.attrs = pattr;
+        pcfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&pcfg, pack_prefix_kernel, a, nb > 0 ? nb : 1)) != cudaSuccess) return e;
     } else {
         pack_scan_kernel<<<1, kScanThreads, 0, stream>>>(a, aux);
     }
