@@ -796,7 +796,30 @@ def pack_measure(ops, dev, name="c5", reps=20):
                        ("the whole call (one fused kernel)" if fused else "the token-stream kernel only", reps)),
             "graph": pack_graph_measure(ops, dev, w, toks_d, lens_d, nbytes, pk.get("hbm_gbs", 6800.0)),
             "graph_16_rows": pack_graph_16_rows(ops, dev, w, toks_d, lens_d, segs, pk.get("hbm_gbs", 6800.0)),
-            "graph_many_docs": pack_graph_many_docs(ops, dev, w, pk.get("hbm_gbs", 6800.0))}
+            "graph_many_docs": pack_graph_many_docs(ops, dev, w, pk.get("hbm_gbs", 6800.0)),
+            "graph_unpack_16x": pack_graph_unpack(ops, dev, pk.get("hbm_gbs", 6800.0))}
+
+
+def pack_graph_unpack(ops, dev, hbm, times=16):
+    """build_unpack (use_packed_dataset=False) on the 32K workload's documents
+    sixteen times over: rows of micro_bsz 4 documents, each cut to SEQ_LEN 8192,
+    then padding. Algorithmic bytes: 4 B read per kept token and per document
+    length, 12 B written per output position, the segment fields."""
+    import torch
+    w, lens, toks = workload_docs("c3_unpack")
+    lens16 = list(lens) * times
+    toks_d = torch.tensor(toks, dtype=torch.int32, device=dev).repeat(times)
+    lens_d = torch.tensor(lens16, dtype=torch.int32, device=dev)
+    rows, _ = ops.pack_rows(len(lens16), toks_d.numel(), w.micro_bsz, w.seq_len, False)
+    npos = rows * w.micro_bsz * w.seq_len
+    kept = sum(min(int(n), w.seq_len) for n in lens16)
+    segs = ops.pack_num_segs(lens16, w.micro_bsz, w.seq_len, False)
+    nbytes = 4 * kept + 4 * len(lens16) + 12 * npos + 4 * (segs + 1) + 4 * (2 * rows + 2)
+    r = pack_graph_measure(ops, dev, w, toks_d, lens_d, nbytes, hbm)
+    r["workload"] = "%d documents (the 32K workload's, %d times over), use_packed_dataset=False, %d rows of %d x %d" % (
+        len(lens16), times, rows, w.micro_bsz, w.seq_len)
+    r["bytes"] = nbytes
+    return r
 
 
 def pack_graph_many_docs(ops, dev, w, hbm):

@@ -205,7 +205,6 @@ __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, i
         const int d = d0 + k;
         if (d < nd) {
             a.doc_out[d] = static_cast<int32_t>(start[k]);
-            a.doc_in[d] = static_cast<int32_t>(start[k]);
             a.aligned[d] = static_cast<int32_t>(frun);
         }
         frun += flag[k];
@@ -224,7 +223,6 @@ __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, i
                 const long long pad = total % plen != 0;
                 const long long num_segs = rows + nd - 1 - tot_al + pad;
                 a.doc_out[nd] = static_cast<int32_t>(total);
-                a.doc_in[nd] = static_cast<int32_t>(total);
                 a.aligned[nd] = static_cast<int32_t>(tot_al);
                 *a.num_segs = static_cast<int32_t>(num_segs);
                 a.row_seg_ptr[rows] = static_cast<int32_t>(num_segs);
@@ -367,56 +365,80 @@ __global__ void __launch_bounds__(kScanThreads) pack_scan_kernel(PackArgs a, int
     }
 }
 
-// build_unpack, per output position: id, label, index. Row r holds documents
-// r * micro_bsz .. +micro_bsz - 1, each truncated to SEQ_LEN, then padding.
-__device__ __forceinline__ void unpack_position(const PackArgs &a, long long p, int32_t &id, int32_t &lab,
-                                                int32_t &idx)
-{
-    const long long plen = a.plen;
-    const long long r = p / plen;
-    const int d0 = static_cast<int>(r * a.micro_bsz);
-    const int d1 = min(a.num_docs, d0 + a.micro_bsz);
-    const int dd = last_le(a.doc_out, d0, d1, p);
-    const long long start = a.doc_out[dd];
-    const int keep = a.doc_keep[dd];
-    const long long t = p - start;
-    if (t < keep) {
-        const long long src = static_cast<long long>(a.doc_in[dd]) + t;
-        id = a.tokens[src];
-        lab = (t + 1 < keep) ? a.tokens[src + 1] : -100;
-        idx = static_cast<int32_t>(t);
-    } else {
-        id = 0;
-        lab = -100;
-        idx = static_cast<int32_t>(t - keep);
-    }
-}
-
+// build_unpack token stream: row r holds documents r * micro_bsz .. +micro_bsz - 1,
+// each truncated to SEQ_LEN and placed one after the other, then padding.
+// kChunk consecutive output positions per CTA, four per thread per iteration.
+// A thread keeps its row and its current document (output start, kept length,
+// input start) in registers: a division where a group of four starts past the
+// row, a search among the row's documents where it starts past the document,
+// and a step to the next document (which starts where the kept part ends)
+// inside a group.
 __global__ void __launch_bounds__(kStreamThreads) unpack_stream_kernel(PackArgs a)
 {
-    const long long npos = static_cast<long long>(a.rows) * a.plen;
-    const long long P0 = static_cast<long long>(blockIdx.x) * kChunk;
-    const long long P1 = min(npos, P0 + kChunk);
+    const int plen = a.plen, mb = a.micro_bsz, nd = a.num_docs;
+    const int npos = a.rows * plen;   // rows * plen <= 2^31 - 65537 is checked on the host
+    const int P0 = static_cast<int>(blockIdx.x) * kChunk;
+    const int P1 = min(npos, P0 + kChunk);
     pdl_wait();
     if (*reinterpret_cast<volatile int *>(a.status) != 0) return;
+    int row_end = 0, d_end = 0;        // the current row's end and its documents' end index
+    int dd = 0, start = 0, keep = 0, src = 0;
+    auto load_doc = [&](int d) {
+        dd = d;
+        start = a.doc_out[d];
+        keep = a.doc_keep[d];
+        src = a.doc_in[d];
+    };
+#pragma unroll
     for (int it = 0; it < kStreamIters; ++it) {
-        long long p = P0 + (static_cast<long long>(it) * kStreamThreads + threadIdx.x) * 4;
+        const int p = P0 + (it * kStreamThreads + threadIdx.x) * 4;
         if (p >= P1) break;
         int32_t id[4], lab[4], idx[4];
-        const int n = static_cast<int>(min(4LL, P1 - p));
+        if (p >= row_end) {                                  // a new row: its documents d0 .. d_end - 1
+            const int r = p / plen;
+            row_end = (r + 1) * plen;
+            const int d0 = r * mb;
+            d_end = min(nd, d0 + mb);
+            load_doc(last_le(a.doc_out, d0, d_end, p));      // doc_out[d0] = r * plen <= p
+        } else if (p - start >= keep && dd + 1 < d_end) {    // past the document: a later one of the row
+            load_doc(last_le(a.doc_out, dd + 1, d_end, p));  // doc_out[dd + 1] = start + keep <= p
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            if (k < n) unpack_position(a, p + k, id[k], lab[k], idx[k]);
-            else id[k] = lab[k] = idx[k] = 0;
+            const int q = p + k;
+            if (q >= P1) {
+                id[k] = lab[k] = idx[k] = 0;
+                continue;
+            }
+            if (q >= row_end) {                              // one position further: the next row's first
+                row_end += plen;
+                const int d0 = d_end;                        // the next row's first document
+                d_end = min(nd, d0 + mb);
+                load_doc(d0);
+            }
+            int t = q - start;
+            if (t >= keep && dd + 1 < d_end) {               // the next document starts where this one's kept part ends
+                load_doc(dd + 1);
+                t = q - start;
+            }
+            if (t < keep) {
+                id[k] = a.tokens[src + t];
+                lab[k] = (t + 1 < keep) ? a.tokens[src + t + 1] : -100;
+                idx[k] = t;
+            } else {                                         // the row's padding tail
+                id[k] = 0;
+                lab[k] = -100;
+                idx[k] = t - keep;
+            }
         }
-        if (a.vec_out && n == 4) {
+        if (a.vec_out && p + 4 <= P1) {
             *reinterpret_cast<int4 *>(a.input_ids + p) = make_int4(id[0], id[1], id[2], id[3]);
             *reinterpret_cast<int4 *>(a.labels + p) = make_int4(lab[0], lab[1], lab[2], lab[3]);
             *reinterpret_cast<int4 *>(a.indexes + p) = make_int4(idx[0], idx[1], idx[2], idx[3]);
         } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                if (k < n) {
+                if (p + k < P1) {
                     a.input_ids[p + k] = id[k];
                     a.labels[p + k] = lab[k];
                     a.indexes[p + k] = idx[k];
