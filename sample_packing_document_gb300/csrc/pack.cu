@@ -9,7 +9,8 @@
 // segment; indexes: position inside the current segment).
 //
 // build_pack with at most 1024 documents and 512 rows runs as one fused
-// launch (pack_fused_kernel). Otherwise, two launches on one stream:
+// launch (pack_fused_kernel), build_unpack with at most 1024 documents as
+// another (unpack_fused_kernel). Otherwise, two launches on one stream:
 //   build_pack:
 //     pack_prefix_kernel  prefix sums of the document lengths (document starts)
 //                         and of the "starts on a row start" flags, 4096
@@ -885,6 +886,185 @@ __global__ void __launch_bounds__(kFusedThreads, 8) pack_fused_kernel(PackArgs a
     }
 }
 
+// build_unpack with at most 1024 documents (so at most 1024 rows): one launch.
+// Every CTA scans the document lengths into shared memory (the raw lengths'
+// prefix gives a document's input start, the kept lengths' prefix its place
+// in its row); CTA 0 then writes the segment fields and the status word,
+// every other CTA 1024 output positions. Same rules and outputs as
+// pack_scan_kernel + unpack_stream_kernel.
+__global__ void __launch_bounds__(kFusedThreads, 8) unpack_fused_kernel(PackArgs a)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    __shared__ int32_t s_in[kFusedDocs + 1];   // input start of each document (+ num_tokens)
+    __shared__ int32_t s_k[kFusedDocs + 1];    // kept tokens before each document (+ all kept)
+    __shared__ int sh[32];
+    __shared__ int bad_s;
+    const int tid = threadIdx.x;
+    const int nd = a.num_docs, mb = a.micro_bsz, plen = a.plen;
+    const int npos = a.rows * plen;   // rows * plen <= 2^31 - 65537 is checked on the host
+    if (tid == 0) bad_s = 0;
+    {
+        int len[4], kp[4];
+        long long sraw = 0;
+        bool bad = false;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = tid * 4 + k;
+            len[k] = d < nd ? a.doc_lens[d] : 0;
+            if (d < nd && len[k] <= 0) bad = true;
+            if (len[k] < 0) len[k] = 0;
+            kp[k] = min(len[k], a.seq_len);
+            sraw += len[k];
+        }
+        // valid lengths sum to num_tokens <= 2^31 - 1, so any partial sum above it is bad
+        if (sraw > a.num_tokens) bad = true;
+        if (bad) atomicOr(&bad_s, 1);
+        int tot_raw, tot_keep;
+        long long eraw = block_excl_scan256(bad ? 0 : static_cast<int>(sraw), &tot_raw, sh);
+        long long ekeep = block_excl_scan256(bad ? 0 : kp[0] + kp[1] + kp[2] + kp[3], &tot_keep, sh);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int d = tid * 4 + k;
+            if (d < nd) {
+                s_in[d] = static_cast<int32_t>(eraw);
+                s_k[d] = static_cast<int32_t>(ekeep);
+            }
+            eraw += len[k];
+            ekeep += kp[k];
+        }
+        if (tid == 0) {
+            s_in[nd] = tot_raw;
+            s_k[nd] = tot_keep;
+            if (tot_raw != a.num_tokens) bad_s = 1;
+        }
+    }
+    __syncthreads();
+    if (bad_s) {
+        if (blockIdx.x == 0 && tid == 0) {
+            *a.status = kErrBadDocs;   // CTA 0 alone owns the status word in this launch
+            *a.num_segs = 0;
+        }
+        return;
+    }
+
+    if (blockIdx.x > 0) {
+        const int p = static_cast<int>(blockIdx.x - 1) * kFusedChunk + tid * 4;
+        if (p >= npos) return;
+        // row r holds documents d0 .. d_end - 1 one after the other, then padding;
+        // the row's documents start at r * plen + s_k[d] - s_k[d0]
+        const int r = p / plen;
+        int row_start = r * plen;
+        int d0 = r * mb, d_end = min(nd, d0 + mb);
+        int base = row_start - s_k[d0];
+        int dd = d0 + last_le_smem(s_k + d0, d_end - d0, p - base);
+        int start = base + s_k[dd], keep = s_k[dd + 1] - s_k[dd];
+        int32_t id[4], lab[4], idx[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q = p + k;
+            if (q >= npos) {
+                id[k] = lab[k] = idx[k] = 0;
+                continue;
+            }
+            if (q >= row_start + plen) {   // one position further: the next row's first
+                row_start += plen;
+                d0 = d_end;
+                d_end = min(nd, d0 + mb);
+                base = row_start - s_k[d0];
+                dd = d0;
+                start = row_start;
+                keep = s_k[dd + 1] - s_k[dd];
+            }
+            int t = q - start;
+            if (t >= keep && dd + 1 < d_end) {   // the next document starts where this one's kept part ends
+                ++dd;
+                start += keep;
+                keep = s_k[dd + 1] - s_k[dd];
+                t = q - start;
+            }
+            if (t < keep) {
+                const int src = s_in[dd] + t;
+                id[k] = __ldg(a.tokens + src);
+                lab[k] = (t + 1 < keep) ? __ldg(a.tokens + src + 1) : -100;
+                idx[k] = t;
+            } else {                             // the row's padding tail
+                id[k] = 0;
+                lab[k] = -100;
+                idx[k] = t - keep;
+            }
+        }
+        if (a.vec_out && p + 4 <= npos) {
+            *reinterpret_cast<int4 *>(a.input_ids + p) = make_int4(id[0], id[1], id[2], id[3]);
+            *reinterpret_cast<int4 *>(a.labels + p) = make_int4(lab[0], lab[1], lab[2], lab[3]);
+            *reinterpret_cast<int4 *>(a.indexes + p) = make_int4(idx[0], idx[1], idx[2], idx[3]);
+        } else {
+            for (int k = 0; k < 4 && p + k < npos; ++k) {
+                a.input_ids[p + k] = id[k];
+                a.labels[p + k] = lab[k];
+                a.indexes[p + k] = idx[k];
+            }
+        }
+        return;
+    }
+
+    // CTA 0: one segment per document, plus the padding tail of every row its
+    // documents do not fill; a row's first segment comes after the documents
+    // and padding tails of the rows before it (all full rows of micro_bsz
+    // documents). max_seqlen per row from shared-memory maxima.
+    __shared__ int32_t s_rsp[kFusedDocs];
+    __shared__ int32_t s_rmax[kFusedDocs];
+    const int rows = a.rows;
+    int f[4], fsum = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = tid * 4 + k;
+        f[k] = 0;
+        if (r < rows) {
+            const int d0 = r * mb, d1 = min(nd, d0 + mb);
+            const int fill = s_k[d1] - s_k[d0];
+            f[k] = fill < plen ? 1 : 0;
+            s_rmax[r] = f[k] ? plen - fill : 0;
+        }
+        fsum += f[k];
+    }
+    int npad;
+    int run = block_excl_scan256(fsum, &npad, sh);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = tid * 4 + k;
+        if (r < rows) s_rsp[r] = r * mb + run;
+        run += f[k];
+    }
+    __syncthreads();
+    const int num_segs = nd + npad;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int d = tid * 4 + k;
+        if (d < nd) {
+            const int r = d / mb, d0 = r * mb;
+            a.cu_seqlens[s_rsp[r] + d - d0] = r * plen + s_k[d] - s_k[d0];
+            atomicMax(&s_rmax[r], s_k[d + 1] - s_k[d]);
+        }
+        const int r = tid * 4 + k;
+        if (r < rows && f[k]) {
+            const int d0 = r * mb, d1 = min(nd, d0 + mb);
+            a.cu_seqlens[s_rsp[r] + d1 - d0] = r * plen + s_k[d1] - s_k[d0];
+        }
+    }
+    __syncthreads();
+    for (int r = tid; r < rows; r += kFusedThreads) {
+        a.max_seqlen[r] = s_rmax[r];
+        a.row_seg_ptr[r] = s_rsp[r];
+    }
+    if (tid == 0) {
+        a.row_seg_ptr[rows] = num_segs;
+        a.cu_seqlens[num_segs] = npos;
+        *a.num_segs = num_segs;
+        *a.status = 0;
+    }
+}
+
 }  // namespace
 
 size_t pack_ws_bytes(int64_t num_docs)
@@ -923,6 +1103,21 @@ cudaError_t launch_pack(const PackArgs &a_in, int num_sms, cudaStream_t stream)
         cfg.numAttrs = 1;
         prof_begin(kProfPackStream, stream);
         cudaError_t e0 = cudaLaunchKernelEx(&cfg, pack_fused_kernel, a);
+        prof_end(kProfPackStream, stream);
+        return e0;
+    }
+    if (!a.packed && a.num_docs >= 1 && a.num_docs <= kFusedDocs) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(1 + (npos + kFusedChunk - 1) / kFusedChunk));
+        cfg.blockDim = dim3(kFusedThreads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        prof_begin(kProfPackStream, stream);
+        cudaError_t e0 = cudaLaunchKernelEx(&cfg, unpack_fused_kernel, a);
         prof_end(kProfPackStream, stream);
         return e0;
     }

@@ -202,6 +202,40 @@ def test_bad_doc_lengths_set_status(ops):
     assert st == 0 and g["num_segs"] == 4 and g["cu_seqlens"].tolist() == [0, 4, 8, 10, 16]
 
 
+@pytest.mark.parametrize("nd_lo,nd_hi", [(1, 1024), (1025, 3000)])
+def test_random_unpack_cases(ops, nd_lo, nd_hi):
+    """build_unpack (use_packed_dataset=False) on both sides of the one-launch
+    limit (1024 documents): documents shorter and longer than SEQ_LEN, a
+    partial last row, row lengths that are not a multiple of four."""
+    rng = np.random.default_rng(77 + nd_lo)
+    for _ in range(30):
+        nd = int(rng.integers(nd_lo, nd_hi + 1))
+        mb, sl = int(rng.integers(1, 6)), int(rng.integers(1, 40))
+        lens = rng.integers(1, 3 * sl + 1, size=nd).astype(np.int32)
+        toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+        st, g = _gpu_pack(ops, toks, lens, mb, sl, False)
+        assert st == 0
+        _assert_same(g, OA.pack(toks, lens, mb, sl, False))
+
+
+@pytest.mark.parametrize("nd", [3, 2000])
+def test_bad_doc_lengths_set_status_unpack(ops, nd):
+    """build_unpack with a zero-length document or lengths that do not sum to
+    num_tokens reports SPD_ERR_BAD_DOCS (one-launch and two-launch paths)."""
+    rng = np.random.default_rng(nd)
+    lens = rng.integers(1, 9, size=nd).astype(np.int32)
+    toks = rng.integers(1, 50000, size=int(lens.sum())).astype(np.int32)
+    bad = lens.copy()
+    bad[nd // 2] = 0
+    st, _ = _gpu_pack(ops, toks[:int(bad.sum())], bad, 2, 8, False)
+    assert st == -7
+    st, _ = _gpu_pack(ops, toks[:-1], lens, 2, 8, False)
+    assert st == -7
+    st, g = _gpu_pack(ops, toks, lens, 2, 8, False)
+    assert st == 0
+    _assert_same(g, OA.pack(toks, lens, 2, 8, False))
+
+
 @pytest.mark.parametrize("n_docs,len_hi,mb,sl", [
     (40000, 8, 1, 65536),        # 10 prefix CTAs chained by the look-back
     (300000, 8, 4, 8192),        # 74 prefix CTAs, many rows, documents split across rows
