@@ -770,7 +770,7 @@ def pack_measure(ops, dev, name="c5", reps=20):
     npos = out["rows"] * w.micro_bsz * w.seq_len
     nbytes = 4 * len(toks) + 4 * len(lens) + 12 * npos + 4 * (segs + 1) + 4 * (2 * out["rows"] + 2)
     times = []
-    fused = w.use_packed_dataset and len(lens) <= 1024
+    fused = len(lens) <= 1024 and (not w.use_packed_dataset or out["rows"] <= 512)   # one-launch paths
     for it in range(reps + 3):
         flush.zero_()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
