@@ -81,7 +81,9 @@ int spd_version(void);
  * the caller) on the launch stream immediately before and after that kernel,
  * so its duration can be read with cudaEventElapsedTime. kernel:
  * SPD_PROFILE_NONE (off), SPD_PROFILE_PACK_STREAM (the token-stream kernel of
- * spd_pack_tokens), SPD_PROFILE_ATTN_FWD / SPD_PROFILE_ATTN_BWD (the main
+ * spd_pack_tokens: its one kernel with at most 1024 documents, and in
+ * build_pack mode at most 512 rows; else the second of its two kernels),
+ * SPD_PROFILE_ATTN_FWD / SPD_PROFILE_ATTN_BWD (the main
  * attention kernel of each call, without the scheduling and pre/post-pass
  * kernels). Null events turn it off. Returns SPD_OK or SPD_ERR_INVALID_ARG.
  */
