@@ -222,7 +222,8 @@ __global__ void __launch_bounds__(kScanThreads) pack_prefix_kernel(PackArgs a, i
             if (tot_len != total) fail = true;
             if (!fail) {
                 const long long pad = total % plen != 0;
-                const long long num_segs = rows + nd - 1 - tot_al + pad;
+                // no documents: no rows and no segments (cu_seqlens = {0})
+                const long long num_segs = rows == 0 ? 0 : rows + nd - 1 - tot_al + pad;
                 a.doc_out[nd] = static_cast<int32_t>(total);
                 a.aligned[nd] = static_cast<int32_t>(tot_al);
                 *a.num_segs = static_cast<int32_t>(num_segs);
