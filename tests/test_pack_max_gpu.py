@@ -1,0 +1,193 @@
+"""The pack at the largest size the ABI accepts: rows * micro_bsz * seq_len
+just below 2^31 - 65537 output positions (positions are 32-bit in the kernels,
+which step up to one chunk past the last position before their bounds
+checks), on each of its four paths: build_pack in one launch (few documents)
+and in two (more than 1024 documents), build_unpack in one launch and in two.
+
+The outputs (25.8 GB) are far too large for the oracle's Python loops, so
+they are checked against closed forms that hold at any size: the tokens are
+t[i] = i mod 49999 + 1, and every output position is described by the
+segment it falls in (its first position, the input position of that first
+token, and the output position where its document's kept tokens end). The
+segment list is built here from the document lengths alone (build_pack: the
+documents end to end, cut at every row start, the padding tail its own
+segment; build_unpack: micro_bsz documents per row, each cut to seq_len, then
+the row's padding), and `test_segment_model_matches_oracle` pins that builder
+to the oracle's build_pack / build_unpack on small random cases, element by
+element.
+"""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import pack as P
+
+LIMIT = 2 ** 31 - 65537
+TOKEN_MOD = 49999
+
+
+def segments(lens, mb, sl, packed):
+    """(first position, end, input position of the first token or None for
+    padding, output end of the document's kept tokens) for every segment, in
+    order, plus the row count and row length."""
+    plen = mb * sl
+    nd = len(lens)
+    total = int(sum(lens))
+    out = []
+    if packed:
+        rows = -(-total // plen)
+        start = 0
+        for n in lens:
+            end = start + int(n)
+            a = start
+            while a < end:                       # cut at every row start inside the document
+                b = min(end, (a // plen + 1) * plen)
+                out.append((a, b, a, end))
+                a = b
+            start = end
+        if total < rows * plen:
+            out.append((total, rows * plen, None, None))
+    else:
+        rows = -(-nd // mb)
+        in_start = np.concatenate([[0], np.cumsum(np.asarray(lens, np.int64))]).astype(np.int64)
+        for r in range(rows):
+            o = r * plen
+            for d in range(r * mb, min(nd, r * mb + mb)):
+                keep = min(int(lens[d]), sl)
+                out.append((o, o + keep, int(in_start[d]), o + keep))
+                o += keep
+            if o < (r + 1) * plen:
+                out.append((o, (r + 1) * plen, None, None))
+    return out, rows, plen
+
+
+def segment_fields(segs, rows, plen):
+    cu = [a for a, _, _, _ in segs] + [rows * plen]
+    rsp, mx = [], [0] * rows
+    i = 0
+    for r in range(rows):
+        while i < len(segs) and segs[i][0] < r * plen:
+            i += 1
+        rsp.append(i)
+    rsp.append(len(segs))
+    for a, b, _, _ in segs:
+        mx[a // plen] = max(mx[a // plen], b - a)
+    return cu, rsp, mx
+
+
+def expected_small(toks, lens, mb, sl, packed):
+    """Every output from the segment model (small cases only)."""
+    segs, rows, plen = segments(lens, mb, sl, packed)
+    n = rows * plen
+    ids, lab, idx = [0] * n, [-100] * n, [0] * n
+    for a, b, src, dend in segs:
+        for p in range(a, b):
+            idx[p] = p - a
+            if src is not None:
+                t = src + (p - a)
+                ids[p] = toks[t]
+                lab[p] = toks[t + 1] if p + 1 < dend else -100
+    cu, rsp, mx = segment_fields(segs, rows, plen)
+    return {"input_ids": ids, "labels": lab, "indexes": idx, "cu_seqlens": cu, "row_seg_ptr": rsp,
+            "max_seqlen": mx, "num_segs": len(segs), "rows": rows}
+
+
+def test_segment_model_matches_oracle():
+    rng = random.Random(271)
+    for packed in (True, False):
+        for _ in range(400):
+            mb, sl = rng.randint(1, 4), rng.randint(1, 12)
+            docs = [[rng.randint(1, 49999) for _ in range(rng.randint(1, 3 * mb * sl))]
+                    for _ in range(rng.randint(1, 9))]
+            toks = [t for d in docs for t in d]
+            got = expected_small(toks, [len(d) for d in docs], mb, sl, packed)
+            ref = P.pack_flat(docs, mb, sl, packed)
+            for key in ("input_ids", "labels", "indexes", "cu_seqlens", "row_seg_ptr", "max_seqlen", "num_segs",
+                        "rows"):
+                assert list(np.atleast_1d(got[key])) == list(np.atleast_1d(ref[key])), (packed, key)
+
+
+# ------------------------------------------------------------------ GPU, at the size limit
+
+def _tokens(n, device):
+    t = torch.empty(n, dtype=torch.int32, device=device)
+    step = 1 << 26
+    for c0 in range(0, n, step):
+        c1 = min(n, c0 + step)
+        t[c0:c1] = (torch.arange(c0, c1, dtype=torch.int64, device=device) % TOKEN_MOD + 1).to(torch.int32)
+    return t
+
+
+def _check_outputs(out, segs, rows, plen):
+    dev = out["input_ids"].device
+    step = 1 << 26
+    for a, b, src, dend in segs:
+        for c0 in range(a, b, step):
+            c1 = min(b, c0 + step)
+            rel = torch.arange(c0 - a, c1 - a, dtype=torch.int64, device=dev)
+            if src is None:
+                ids = torch.zeros_like(rel)
+                lab = torch.full_like(rel, -100)
+            else:
+                t = rel + src
+                ids = t % TOKEN_MOD + 1
+                lab = (t + 1) % TOKEN_MOD + 1
+                if c0 <= dend - 1 < c1:           # the document's last kept token
+                    lab[dend - 1 - c0] = -100
+            assert torch.equal(out["input_ids"][c0:c1], ids.to(torch.int32)), ("input_ids", a, c0)
+            assert torch.equal(out["labels"][c0:c1], lab.to(torch.int32)), ("labels", a, c0)
+            assert torch.equal(out["indexes"][c0:c1], rel.to(torch.int32)), ("indexes", a, c0)
+    cu, rsp, mx = segment_fields(segs, rows, plen)
+    ns = int(out["num_segs"].item())
+    assert ns == len(segs)
+    assert out["cu_seqlens"][:ns + 1].cpu().tolist() == cu
+    assert out["row_seg_ptr"][:rows + 1].cpu().tolist() == rsp
+    assert out["max_seqlen"][:rows].cpu().tolist() == mx
+
+
+def _case(name):
+    rng = np.random.default_rng(1234)
+    if name == "pack_one_launch":
+        mb, sl, packed = 1, LIMIT // 2, True
+        total = 2 * sl - 5                                  # a 5-token padding tail
+        lens = [1, sl - 1, 123456789, 1]                    # the third document starts on row 1's start
+        lens.append(total - sum(lens))
+    elif name == "pack_two_launches":
+        mb, sl, packed = 1, LIMIT // 2, True
+        total = 2 * sl - 3
+        lens = rng.integers(1, 2_000_000, size=1499).tolist()
+        lens.append(total - sum(lens))
+    elif name == "unpack_one_launch":
+        mb, sl, packed = 2, LIMIT // 4, False
+        lens = [sl + 7, 3, sl, 100]                         # cut, short, exact, short (padded row)
+    else:                                                   # unpack_two_launches
+        mb, packed = 1024, False
+        sl = LIMIT // (2 * mb)
+        lens = rng.integers(1, sl + sl // 4, size=2048).tolist()
+    assert mb * sl * (-(-sum(lens) // (mb * sl)) if packed else -(-len(lens) // mb)) <= LIMIT
+    return lens, mb, sl, packed
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["pack_one_launch", "pack_two_launches", "unpack_one_launch",
+                                  "unpack_two_launches"])
+def test_pack_at_the_position_limit(name):
+    from sample_packing_document_gb300 import build, ops
+    build.build()
+    ops.load()
+    lens, mb, sl, packed = _case(name)
+    segs, rows, plen = segments(lens, mb, sl, packed)
+    assert rows * plen > LIMIT - 4 * mb * sl // 1000     # within a fraction of a row of the limit
+    dev = "cuda"
+    toks = _tokens(int(sum(lens)), dev)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    out = ops.alloc_pack_outputs(len(lens), toks.numel(), mb, sl, packed, dev)
+    assert out["rows"] == rows
+    ops.pack_tokens(toks, lens_d, mb, sl, packed, out=out)
+    assert ops.read_status(out["ws"]) == 0
+    del toks
+    _check_outputs(out, segs, rows, plen)
+    del out
+    torch.cuda.empty_cache()
