@@ -17,7 +17,9 @@ def _ops():
     return ops
 
 
-@pytest.mark.parametrize("T,V,seed", [(200, 50000, 0), (64, 1001, 1), (3, 7, 2), (1024, 4096, 3)])
+@pytest.mark.parametrize("T,V,seed", [(200, 50000, 0), (64, 1001, 1), (3, 7, 2), (1024, 4096, 3),
+                                      (5, 1, 4), (9, 2, 5), (1, 8, 6), (1, 50000, 7),   # one class, two, one token
+                                      (40, 131072, 8)])                               # larger than the smem row path
 def test_loss_and_gradient_match_oracle(T, V, seed):
     ops = _ops()
     g = torch.Generator().manual_seed(seed)

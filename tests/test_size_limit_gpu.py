@@ -1,8 +1,11 @@
-"""The pack at the largest size the ABI accepts: rows * micro_bsz * seq_len
-just below 2^31 - 65537 output positions (positions are 32-bit in the kernels,
-which step up to one chunk past the last position before their bounds
-checks), on each of its four paths: build_pack in one launch (few documents)
-and in two (more than 1024 documents), build_unpack in one launch and in two.
+"""The pack and the data steps at the largest size the ABI accepts: rows x
+row length just below 2^31 - 65537 positions (positions are 32-bit in the
+kernels, which step up to one chunk past the last position before their
+bounds checks). The pack on each of its four paths: build_pack in one launch
+(few documents) and in two (more than 1024 documents), build_unpack in one
+launch and in two; then the sequence split (three tensors, 16-byte and
+scalar paths), the sequence-parallel padding (a filled and a counting kind)
+and unpack_data.
 
 The outputs (25.8 GB) are far too large for the oracle's Python loops, so
 they are checked against closed forms that hold at any size: the tokens are
@@ -190,4 +193,100 @@ def test_pack_at_the_position_limit(name):
     del toks
     _check_outputs(out, segs, rows, plen)
     del out
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ data steps at the size limit
+
+def _closed(lo, hi, device, plus=1):
+    """t[i] = i mod 49999 + plus for i in [lo, hi) (int32)."""
+    return (torch.arange(lo, hi, dtype=torch.int64, device=device) % TOKEN_MOD + plus).to(torch.int32)
+
+
+def _filled(shape, device, plus=1):
+    t = torch.empty(shape, dtype=torch.int32, device=device)
+    flat, step = t.view(-1), 1 << 26
+    for c0 in range(0, flat.numel(), step):
+        c1 = min(flat.numel(), c0 + step)
+        flat[c0:c1] = _closed(c0, c1, device, plus)
+    return t
+
+
+def _ops():
+    from sample_packing_document_gb300 import build, ops
+    build.build()
+    ops.load()
+    return ops
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("vec", [True, False])
+def test_split_at_the_position_limit(vec):
+    ops, dev, sp, rank, rows = _ops(), "cuda", 8, 5, 2
+    n = (LIMIT // rows) // 32 * 32 - (0 if vec else 8)   # chunk n / 8: a multiple of 4 (16-byte path) or odd
+    assert ((n // sp) % 4 == 0) == vec and rows * n <= LIMIT
+    src = _filled((rows, n), dev)
+    outs = ops.split_sequence_parallel([src, src, src], sp, rank)
+    c = n // sp
+    for o in outs:
+        for r in range(rows):
+            for c0 in range(0, c, 1 << 26):
+                c1 = min(c, c0 + (1 << 26))
+                lo = r * n + rank * c
+                assert torch.equal(o[r, c0:c1], _closed(lo + c0, lo + c1, dev)), (r, c0)
+    del src, outs
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.gpu
+def test_pad_at_the_position_limit():
+    ops, dev, sp, rows = _ops(), "cuda", 8, 2
+    n = LIMIT // rows - 13
+    padded = -(-n // sp) * sp
+    assert rows * padded <= LIMIT and padded > n
+    src = _filled((rows, n), dev)
+    _, lab, pos, _ = ops.pad_for_sequence_parallel(sp, labels=src, position_ids=src)
+    for r in range(rows):
+        for c0 in range(0, n, 1 << 26):
+            c1 = min(n, c0 + (1 << 26))
+            want = _closed(r * n + c0, r * n + c1, dev)
+            assert torch.equal(lab[r, c0:c1], want) and torch.equal(pos[r, c0:c1], want), (r, c0)
+        extra = padded - n
+        assert lab[r, n:].tolist() == [-100] * extra
+        assert pos[r, n:].tolist() == list(range(extra))
+    del src, lab, pos
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.gpu
+def test_unpack_data_at_the_position_limit():
+    """Packed rows of 2 x seq_len: row 0 holds a 1000-token document, one of
+    seq_len + 3 (cut to seq_len) and padding; row 1 one seq_len document and a
+    padding segment of seq_len. Output row (r, m) is segment m of row r cut to
+    seq_len, then 0 / -100 (the oracle's unpack_data rule)."""
+    ops, dev, mb = _ops(), "cuda", 2
+    sl = LIMIT // 4
+    plen, rows = mb * sl, 2
+    cu = [0, 1000, 1000 + sl + 3, plen, plen + sl, 2 * plen]
+    rsp = [0, 3, 5]
+    ids = _filled((rows * plen,), dev)
+    lab = _filled((rows * plen,), dev, plus=2)
+    o_ids, o_lab = ops.unpack_data(ids, lab, torch.tensor(cu, dtype=torch.int32, device=dev),
+                                   torch.tensor(rsp, dtype=torch.int32, device=dev), rows, mb, sl)
+    del ids, lab
+    for r in range(rows):
+        for m in range(mb):
+            s_ = rsp[r] + m
+            a, n = (cu[s_], min(cu[s_ + 1] - cu[s_], sl)) if s_ < rsp[r + 1] else (0, 0)
+            for c0 in range(0, sl, 1 << 26):
+                c1 = min(sl, c0 + (1 << 26))
+                k = max(0, min(c1, n) - c0)               # copied positions in [c0, c1)
+                want_i = torch.zeros(c1 - c0, dtype=torch.int32, device=dev)
+                want_l = torch.full((c1 - c0,), -100, dtype=torch.int32, device=dev)
+                if k:
+                    want_i[:k] = _closed(a + c0, a + c0 + k, dev)
+                    want_l[:k] = _closed(a + c0, a + c0 + k, dev, plus=2)
+                assert torch.equal(o_ids[r, m, c0:c1], want_i), (r, m, c0)
+                assert torch.equal(o_lab[r, m, c0:c1], want_l), (r, m, c0)
+    del o_ids, o_lab
     torch.cuda.empty_cache()
