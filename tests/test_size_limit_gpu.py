@@ -290,3 +290,62 @@ def test_unpack_data_at_the_position_limit():
                 assert torch.equal(o_lab[r, m, c0:c1], want_l), (r, m, c0)
     del o_ids, o_lab
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ attention past 2^31 elements
+
+def _u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.gpu
+def test_attention_past_2_31_elements():
+    """q / out / dO / dQ of 2 heads and k / v / dK / dV of 1 head over
+    2^24 + 2^16 tokens: more than 2^31 elements per tensor, so every element
+    offset needs 64 bits (q's pass 2^31 at token 2^23, k's at token 2^24).
+    Documents of 96-160 tokens keep the work small; bf16 gradients (the
+    benchmarked form). The segments at the start, across both 2^31-element
+    offsets and at the end are compared whole with the fp64 oracle at the
+    attention bars, and every output is finite."""
+    from oracle import attention as OA
+    from sample_packing_document_gb300 import workloads as W
+    ops = _ops()
+    Hq, Hkv, d = 2, 1, 128
+    T = (1 << 24) + (1 << 16)
+    rng = np.random.default_rng(2024)
+    lens = rng.integers(96, 161, size=T // 96 + 1)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    cu = cu[cu < T]
+    cu = np.append(cu, T).astype(np.int64)
+    assert T * Hq * d > 2 ** 32 and T * Hkv * d > 2 ** 31
+    ns = len(cu) - 1
+    q, k, v, do = W.qkv(T, Hq, Hkv, d, 77, device="cuda")
+    cu_d = torch.tensor(cu.astype(np.int32), device="cuda")
+    ws_f = ops.workspace(ops.attn_workspace_size(T, ns, Hq, Hkv, d, False))
+    out, lse = ops.varlen_attn_fwd(q, k, v, cu_d, ns, ws=ws_f)
+    assert ops.read_status(ws_f) == 0
+    del ws_f
+    ws_b = ops.workspace(ops.attn_workspace_size(T, ns, Hq, Hkv, d, True))
+    dq, dk, dv = ops.varlen_attn_bwd(q, k, v, out, do, lse, cu_d, ns, grad_dtype=torch.bfloat16, ws=ws_b)
+    assert ops.read_status(ws_b) == 0
+    del ws_b
+    for t in (out, dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    assert bool(torch.isfinite(lse).all())
+    pick = {0, 1, ns - 2, ns - 1}
+    for tok in (1 << 23, 1 << 24):                    # the segments around each 2^31-element offset
+        s = int(np.searchsorted(cu, tok, side="right")) - 1
+        pick |= {s - 1, s, s + 1}
+    for s in sorted(pick):
+        a, b = int(cu[s]), int(cu[s + 1])
+        sub = [np.asarray([0, b - a], np.int32)]
+        qs, ks, vs, ds = _u16(q[a:b]), _u16(k[a:b]), _u16(v[a:b]), _u16(do[a:b])
+        o_ref, lse_ref = OA.attn_fwd(qs, ks, vs, sub[0])
+        gq, gk, gv, _ = OA.attn_bwd(qs, ks, vs, ds, sub[0])
+        o_gpu = out[a:b].float().cpu().numpy().transpose(1, 0, 2)
+        assert np.max(np.abs(o_gpu - o_ref)) <= 2e-2, s
+        assert np.max(np.abs(lse[:, a:b].cpu().numpy() - lse_ref)) <= 1e-3, s
+        for g, ref in ((dq, gq), (dk, gk), (dv, gv)):
+            assert np.max(np.abs(g[a:b].float().cpu().numpy() - ref)) <= 5e-2, s
+    del q, k, v, do, out, lse, dq, dk, dv
+    torch.cuda.empty_cache()
