@@ -154,3 +154,24 @@ def test_fused_rope_full_size_sampled(ops):
         h, i = divmod(int(it), T)
         assert float(np.abs(o[i, h] - o_ref[n]).max()) <= TOL_O
         assert abs(float(l[h, i]) - lse_ref[n]) <= TOL_LSE
+
+
+@pytest.mark.parametrize("block", range(4))
+def test_fused_rope_random_problems(ops, block):
+    """A seeded sweep: 1-8 segments with lengths at the tile edges or uniform
+    below 1500, GQA groups 1, 2, 3, 7, head_dim 64 / 128, rope_theta from 10^2
+    to 10^6; every output against the oracle's rotation then attention."""
+    rng = np.random.default_rng(7100 + block)
+    edges = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257]
+    heads = [(1, 1), (2, 2), (2, 1), (6, 2), (7, 1)]
+    for case in range(10):
+        nseg = int(rng.integers(1, 9))
+        lens = [int(rng.choice(edges)) if rng.random() < 0.5 else int(rng.integers(1, 1500)) for _ in range(nseg)]
+        Hq, Hkv = heads[int(rng.integers(len(heads)))]
+        d = 64 if rng.random() < 0.4 else 128
+        theta = float(10.0 ** rng.uniform(2, 6))
+        cu, q, k, v, out, lse = _run(ops, lens, Hq, Hkv, d, theta, seed=300 + 10 * block + case)
+        o_ref, lse_ref = _reference(q, k, v, cu, theta)
+        what = (block, case, lens, Hq, Hkv, d, theta)
+        assert float(np.abs(out.float().cpu().numpy().transpose(1, 0, 2) - o_ref).max()) <= TOL_O, what
+        assert float(np.abs(lse.cpu().numpy() - lse_ref).max()) <= TOL_LSE, what

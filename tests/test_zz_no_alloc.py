@@ -77,3 +77,28 @@ def test_noalloc_rejects_oversize_and_reports_bad_seqlens():
     assert _call_noalloc(lib, q, q, q, cu, 3, out, lse, status) == 0
     torch.cuda.synchronize()
     assert int(status.item()) == -4
+
+
+def test_noalloc_random_problems_equal_the_workspace_entry_point():
+    """A seeded sweep of problems on the shared fixed scratch, back to back:
+    the output equals the workspace entry point's bit for bit every time."""
+    from sample_packing_document_gb300 import workloads as W
+    lib, ops = _lib()
+    rng = np.random.default_rng(4242)
+    for case in range(30):
+        nseg = int(rng.integers(1, 12))
+        lens = rng.integers(1, 2000, size=nseg).tolist()
+        Hq, Hkv = [(1, 1), (4, 2), (7, 1), (4, 4)][int(rng.integers(4))]
+        d = 64 if rng.random() < 0.4 else 128
+        cu_h = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        T = int(cu_h[-1])
+        q, k, v, _ = W.qkv(T, Hq, Hkv, d, seed=600 + case, device="cuda")
+        cu = torch.tensor(cu_h, device="cuda")
+        out_ref, lse_ref = ops.varlen_attn_fwd(q, k, v, cu, nseg)
+        out = torch.full_like(q, float("nan"))
+        lse = torch.full((Hq, T), float("nan"), device="cuda")
+        status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+        assert _call_noalloc(lib, q, k, v, cu, nseg, out, lse, status) == 0
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(out, out_ref) and torch.equal(lse, lse_ref), (case, lens, Hq, Hkv, d)
