@@ -154,6 +154,7 @@ __global__ void __launch_bounds__(kRowThreads) loss_row_smem_kernel(LossArgs a)
     __syncthreads();
     uint32_t loads = 0;
     int dummy_status = 0;
+    bool timed_out = false;
     for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
         const int32_t lab = a.labels[t];
         uint16_t *grow = a.dlogits ? a.dlogits + static_cast<size_t>(t) * a.V : nullptr;
@@ -172,7 +173,10 @@ __global__ void __launch_bounds__(kRowThreads) loss_row_smem_kernel(LossArgs a)
         // bounded wait; a copy that never lands leaves the row's loss at 0
         const bool ok = mbar_wait(&bar, loads & 1, &abort_flag, a.status ? a.status : &dummy_status);
         ++loads;
-        if (!__syncthreads_and(ok)) break;
+        if (!__syncthreads_and(ok)) {
+            timed_out = true;
+            break;
+        }
         float m = -INFINITY, s = 0.f;
         for (int i = tid * 8; i < a.V; i += kRowThreads * 8) {
             const uint4 w = *reinterpret_cast<const uint4 *>(srow + i);
@@ -226,6 +230,13 @@ __global__ void __launch_bounds__(kRowThreads) loss_row_smem_kernel(LossArgs a)
             }
         }
         __syncthreads();   // the next row's copy overwrites the staged row
+    }
+    // The copy that timed out may still land: its issuing thread waits for it
+    // once more (bounded) so the CTA's shared memory outlives it.
+    if (timed_out && tid == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&bar, (loads - 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
     }
 }
 
