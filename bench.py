@@ -412,14 +412,17 @@ def workload_config(w, seg_lens):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c5")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of the job (one process each under torchrun; independent replicas)")
+    ap.add_argument("--steps", type=int, default=10, help="timed steps")
+    ap.add_argument("--warmup", type=int, default=3, help="untimed warm-up steps before them")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"],
+                    help="ours: the library on the GPU; reference: the fp64 oracle on this host's cores")
+    ap.add_argument("--workload", default="c5",
+                    help="the step's workload (default: the 1,048,576-token stress row)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle's CPU timing")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the three other workloads' step timings")
     ap.add_argument("--only", choices=["pack", "data"], default=None,
                     help="run only the pack (c5 documents) or the data-step measurements and print their JSON "
                          "(for profiling those kernels without the attention step)")
