@@ -426,6 +426,7 @@ int spd_pad_for_sequence_parallel(const int32_t *src, int32_t *dst, int64_t rows
     a.value = pad_value;
     a.count = count_positions ? 1 : 0;
     a.vec = aligned(dst, 16) ? 1 : 0;
+    a.vec_src = aligned(src, 16) ? 1 : 0;
     return cuda_rc(launch_pad(a, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -4,10 +4,14 @@
 //                                 segment (document) per output row, cut to
 //                                 seq_len, padded with 0 / -100;
 //   split_data_sequence_parallel  the rank's contiguous 1/sp_size chunk of the
-//                                 sequence dimension of each row.
-// Both are pure data movement (HBM-bound): every thread takes groups of four
+//                                 sequence dimension of each row;
+// and pad_for_sequence_parallel (XTuner page "Sequence parallel training of
+// extremely long sequences", sequence parallel API): each row padded at its
+// end to a multiple of sp_size.
+// All are pure data movement (HBM-bound): every thread takes groups of four
 // consecutive output positions, grid-stride, with 16-byte stores where the
-// output row layout allows.
+// output row layout allows (and, for the padding, 16-byte loads realigned
+// across the warp where a row's source start is not).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -121,6 +125,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(SplitArgs a)
 __global__ void __launch_bounds__(kThreads) pad_kernel(PadArgs a)
 {
     const int32_t total = a.rows * a.padded;
+    const int lane = threadIdx.x & 31;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads * 4;
     // Two groups of four output positions per thread and iteration, all eight
     // loads issued before the stores. 64-bit loop index: the step past the last
@@ -131,6 +136,42 @@ __global__ void __launch_bounds__(kThreads) pad_kernel(PadArgs a)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int64_t xu = xl + u * stride;
+            // A warp's 128 consecutive outputs [X, X + 128) inside one row and
+            // before its padding tail come from 128 consecutive source values:
+            // one aligned 16-byte load per lane (plus the next vector for lane
+            // 31) realigned by the warp-uniform shift with a shuffle. Every input
+            // below is the same on all lanes, and X + 128 <= total keeps all of
+            // them in this iteration, so the shuffles see the whole warp.
+            const int64_t X = xu - 4 * lane;
+            bool fast = a.vec && a.vec_src && X + 128 <= total;
+            int32_t r0 = 0, j0 = 0;
+            if (fast) {
+                r0 = static_cast<int32_t>(X / a.padded);
+                j0 = static_cast<int32_t>(X - static_cast<int64_t>(r0) * a.padded);
+                fast = j0 + 128 <= a.len;
+            }
+            const int64_t S = static_cast<int64_t>(r0) * a.len + j0;   // source of output X
+            const int64_t B = S & ~3ll;
+            const int sh = static_cast<int>(S & 3);
+            if (fast && sh && B + 132 > static_cast<int64_t>(a.rows) * a.len) fast = false;
+            if (fast) {
+                const int4 mine = *reinterpret_cast<const int4 *>(a.src + B + 4 * lane);
+                int4 nxt;
+                nxt.x = __shfl_down_sync(0xffffffffu, mine.x, 1);
+                nxt.y = __shfl_down_sync(0xffffffffu, mine.y, 1);
+                nxt.z = __shfl_down_sync(0xffffffffu, mine.z, 1);
+                if (lane == 31 && sh) nxt = *reinterpret_cast<const int4 *>(a.src + B + 128);
+                if (sh == 0) {
+                    v[u][0] = mine.x; v[u][1] = mine.y; v[u][2] = mine.z; v[u][3] = mine.w;
+                } else if (sh == 1) {
+                    v[u][0] = mine.y; v[u][1] = mine.z; v[u][2] = mine.w; v[u][3] = nxt.x;
+                } else if (sh == 2) {
+                    v[u][0] = mine.z; v[u][1] = mine.w; v[u][2] = nxt.x; v[u][3] = nxt.y;
+                } else {
+                    v[u][0] = mine.w; v[u][1] = nxt.x; v[u][2] = nxt.y; v[u][3] = nxt.z;
+                }
+                continue;
+            }
             // the row of the group's first position; a group crosses at most into the next row
             const int32_t x = xu < total ? static_cast<int32_t>(xu) : total;
             int32_t r = x / a.padded, j = x - r * a.padded;

@@ -107,6 +107,7 @@ struct PadArgs {
     int32_t value;                         // fill of the added positions ...
     int count;                             // ... or 1: they count 0, 1, 2, ...
     int vec;                               // 1: 16-byte stores (aligned dst)
+    int vec_src;                           // 1: src is 16-byte aligned
 };
 cudaError_t launch_pad(const PadArgs &a, int num_sms, cudaStream_t stream);
 

@@ -98,7 +98,8 @@ def test_split_random_matches_oracle(rows, length, sp):
 
 
 @pytest.mark.parametrize("rows,length,sp", [(1, 13, 8), (3, 24, 8), (5, 1001, 4), (2, 4093, 8), (7, 30, 1),
-                                             (1, 1, 5), (4, 0, 3), (2, 15, 16)])
+                                             (1, 1, 5), (4, 0, 3), (2, 15, 16),
+                                             (9, 4099, 8), (6, 70001, 16), (5, 256, 8)])   # every source shift of a row
 def test_pad_for_sequence_parallel_matches_oracle(rows, length, sp):
     """Every tensor kind, ragged and already-divisible lengths, the empty row,
     sp_size larger than the row; then the page's purpose: the padded rows split
@@ -138,7 +139,8 @@ def test_pad_full_size_row():
 
 def test_pad_1d_and_unaligned_output():
     """A [len] tensor, and an output view that is not 16-byte aligned (the
-    scalar store path)."""
+    scalar store path); a source view that is not 16-byte aligned (the scalar
+    load path) over rows long enough for the vector path otherwise."""
     ops = _ops()
     x = torch.arange(1, 11, dtype=torch.int32, device="cuda")
     (y,) = [t for t in ops.pad_for_sequence_parallel(4, labels=x) if t is not None]
@@ -149,6 +151,12 @@ def test_pad_1d_and_unaligned_output():
     assert rc == 0
     torch.cuda.synchronize()
     assert buf[1:13].cpu().tolist() == list(range(1, 11)) + [0, 1] and int(buf[0]) == 0 and int(buf[13]) == 0
+    rows, n, sp = 3, 1001, 8
+    base = torch.arange(rows * n + 1, dtype=torch.int32, device="cuda")
+    src = base[1:].view(rows, n)                           # 4 bytes past an aligned start
+    (z,) = [t for t in ops.pad_for_sequence_parallel(sp, labels=src) if t is not None]
+    want = np.array([P.pad_for_sequence_parallel(row.tolist(), sp, "labels") for row in src.cpu().numpy()])
+    assert np.array_equal(z.cpu().numpy(), want)
 
 
 def test_split_rejects_a_length_that_does_not_divide():
