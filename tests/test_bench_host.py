@@ -44,6 +44,17 @@ def test_committed_traffic_record_is_well_formed():
     assert rec["dram_bytes"] == rec["dram_read_bytes"] + rec["dram_write_bytes"]
 
 
+def test_committed_traffic_record_matches_the_current_sources():
+    """The bench reports roofline.traffic only while the backward kernel's
+    sources hash to the recorded value: a source change must come with a new
+    capture, or the reported traffic goes null."""
+    from sample_packing_document_gb300 import workloads as W
+    rec = json.load(open(bench.TRAFFIC_RECORD))
+    assert rec["source"] == bench.kernel_source_hash(bench.BWD_SOURCES)
+    assert bench.recorded_traffic(bench.TRAFFIC_RECORD, bench.BWD_SOURCES, W.WORKLOADS["c5"]) == \
+        rec["dram_bytes"] * W.WORKLOADS["c5"].Hq
+
+
 def test_replica_value_is_the_whole_job():
     assert bench.replica_value(4, 2e12, 1000.0) == pytest.approx(4 * 2e12 / 1.0 / 1e12)
 
