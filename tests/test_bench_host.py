@@ -3,7 +3,6 @@ uses equal the oracle's packing of the same documents, the traffic record is
 reported only for the kernel sources and workload it was captured on, and the
 CPU oracle table runs."""
 import json
-import os
 
 import numpy as np
 import pytest
