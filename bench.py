@@ -54,7 +54,7 @@ def peaks():
 
 # Sources the main backward kernel is compiled from: a recorded DRAM-traffic
 # figure is reported only while their hash matches the one the capture recorded.
-BWD_SOURCES = ("attn_bwd.cu", "ptx.cuh", "internal.h")
+BWD_SOURCES = ("attn_bwd.cu", "ptx.cuh", "internal.h", "sched.cu")   # the schedule shapes the traffic too
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "attn_bwd_traffic.json")
 
 
