@@ -377,3 +377,35 @@ def test_schedule_visits_exactly_the_unmasked_tiles(ops, lens, blocks_per_head, 
         if pairs is not None:
             assert sum(kept) == pairs
         assert sum(kept) == sum(L * (L + 1) // 2 for L in lens)
+
+
+def test_paired_backward_units_full_compare(ops):
+    """Random document lengths of 2100-2900 tokens (17-23 kv tiles) with enough
+    heads that the backward schedule pairs their kv tiles p and n - 1 - p into
+    one unit (the second walking its q tiles downward): the schedule read back
+    holds pairs, and every output element of the forward and of both gradient
+    forms (bf16 and fp32) meets the bars against the oracle."""
+    rng = np.random.default_rng(808)
+    lens = rng.integers(2100, 2901, size=3).tolist()
+    Hq = Hkv = 48
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    q, k, v, do = _inputs(T, Hq, Hkv, 64, 12)
+    cu_t = torch.tensor(cu, device="cuda")
+    ws_b = ops.workspace(ops.attn_workspace_size(T, len(lens), Hq, Hkv, 64, True))
+    out, lse = ops.varlen_attn_fwd(q, k, v, cu_t, len(lens))
+    g32 = ops.varlen_attn_bwd(q, k, v, out, do, lse, cu_t, len(lens), grad_dtype=torch.float32, ws=ws_b)
+    assert ops.read_status(ws_b) == 0
+    units = ops.read_schedule(ws_b)
+    assert ((units[:, 2] & SINGLE) == 0).sum() > 0            # paired units were scheduled
+    g16 = ops.varlen_attn_bwd(q, k, v, out, do, lse, cu_t, len(lens), grad_dtype=torch.bfloat16, ws=ws_b)
+    assert ops.read_status(ws_b) == 0
+    qn, kn, vn, don = _u16(q), _u16(k), _u16(v), _u16(do)
+    o_ref, lse_ref = OA.attn_fwd(qn, kn, vn, cu)
+    assert _maxerr(out.float().cpu().numpy().transpose(1, 0, 2), o_ref) <= TOL_O
+    assert _maxerr(lse.cpu().numpy(), lse_ref) <= TOL_LSE
+    refs = OA.attn_bwd(qn, kn, vn, don, cu)[:3]
+    for g, ref in zip(g32, refs):
+        assert _maxerr(g.cpu().numpy(), ref) <= TOL_G
+    for g, ref in zip(g16, refs):
+        assert _maxerr(g.float().cpu().numpy(), ref) <= TOL_G
