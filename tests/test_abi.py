@@ -31,6 +31,49 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(ops.SIGNATURES)
 
 
+def _prototypes():
+    """name -> (return type, [parameter types]) of every declaration in spd.h."""
+    text = open(os.path.join(ROOT, "include", "spd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for ret, name, params in re.findall(r"([A-Za-z_][\w\s\*]*?)\s*\b(spd_[a-z_0-9]+)\s*\(([^)]*)\)\s*;", text):
+        ps = [] if params.strip() in ("", "void") else [p.strip() for p in params.split(",")]
+        types = []
+        for p_ in ps:
+            p_ = re.sub(r"\bconst\b", "", p_)
+            if "*" in p_:
+                types.append("*")
+            else:
+                types.append(p_.split()[0])            # the type; the name follows it
+        out[name] = (" ".join(ret.replace("const", "").split()), types)
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """The ctypes argument and return types of every entry point follow its C
+    prototype: pointers (and spd_stream_t) as pointers, int64_t / int32_t /
+    int / float / size_t as the same widths."""
+    from sample_packing_document_gb300 import ops
+    width = {"int64_t": ctypes.c_int64, "int32_t": ctypes.c_int32, "int": ctypes.c_int, "float": ctypes.c_float,
+             "size_t": ctypes.c_size_t}
+    protos = _prototypes()
+    assert set(protos) == set(ops.SIGNATURES)
+    for name, (ret, params) in protos.items():
+        res, args = ops.SIGNATURES[name]
+        assert len(args) == len(params), name
+        for i, (c_type, py_type) in enumerate(zip(params, args)):
+            if c_type in ("*", "spd_stream_t"):
+                assert py_type is ctypes.c_void_p or issubclass(py_type, ctypes._Pointer), (name, i)
+            else:
+                assert ctypes.sizeof(py_type) == ctypes.sizeof(width[c_type]) and \
+                    (py_type is ctypes.c_float) == (c_type == "float"), (name, i, c_type, py_type)
+        if ret.endswith("*"):
+            assert res is ctypes.c_char_p, name
+        else:
+            assert ctypes.sizeof(res) == ctypes.sizeof(width[ret]), name
+
+
 def test_read_schedule_host_checks(lib):
     """spd_attn_read_schedule refuses null pointers before touching a GPU."""
     n = ctypes.c_int32(0)
